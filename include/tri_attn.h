@@ -1,0 +1,167 @@
+/*
+ * tri_attn.h -- C ABI of the B300 gated triangle self-attention library.
+ *
+ * The operation (pair-biased, gated triangle self-attention over a pair
+ * representation Z[I, I, c_z]):
+ *
+ *   zh      = LayerNorm(Z)                         per pair vector, biased variance
+ *   q, k, v = zh W_q, zh W_k, zh W_v               H heads x d channels, no bias
+ *   g       = sigmoid(zh W_g + b_g)                H*d channels
+ *   b[h]    = zh W_b[:, h]                         one pair bias per head
+ *   starting node, row i, head h, query (i, j), keys (i, k) with mask[k] = 1:
+ *     o[i,j,h] = sum_k softmax_k( q[i,j,h].k[i,k,h] / sqrt(d) + b[h,j,k] ) v[i,k,h]
+ *   ending node, column j, head h, query (i, j), keys (k, j) with mask[k] = 1:
+ *     o[i,j,h] = sum_k softmax_k( q[i,j,h].k[k,j,h] / sqrt(d) + b[h,k,i] ) v[k,j,h]
+ *   out[i,j] = (g[i,j] * concat_h o[i,j,h]) W_o + b_o,   and 0 where mask[i]*mask[j] = 0.
+ *
+ * Sources.  None of the pages prints these formulas; they name the parts:
+ *   - "戴尔PowerEdgeXE8545 强劲算力助力蛋白质模型分析" (Dell), Evoformer paragraph:
+ *     the Evoformer processes the residue-pair graph with triangle attention.
+ *   - "通量提升达 23.11 倍！至强可扩展平台助力 AlphaFold2 端到端优化" (Intel),
+ *     step 2 (triangle-geometry constraints learnt by self-attention over the
+ *     pair representation) and step 4 (the attention module carries a large
+ *     bias term formed by tensor contractions; fusing the score contraction
+ *     with the bias add).
+ *   - "Efficient protein structure prediction ... with OpenFold-TRT",
+ *     Methodology: a bf16 Evoformer core and fused kernels.
+ *   - "Resumo Técnico: Design-CP", Methodology 1: scores formed on the fly
+ *     from key/value pieces, never materialising the full score matrix, and
+ *     self-attention recast as cross-attention over key shards (the key-chunk
+ *     schedule selected by tri_attn_config.key_chunks).
+ * Readings where the pages are silent: LayerNorm eps from the config (1e-5
+ * by default), biased variance; no bias on the q/k/v/pair-bias projections;
+ * the 1/sqrt(d) scale applies to q.k only; masked keys get -inf; pairs that
+ * touch a padded token are written as exactly 0 (a fully masked row is 0,
+ * never NaN); the caller adds any residual.
+ *
+ * Conventions for every entry point
+ *   - Tensors are caller-owned DEVICE memory unless stated otherwise; the
+ *     library never frees them and keeps no pointer after a call returns.
+ *   - Weights are stored [in, out] row-major (x W); head h owns channels
+ *     h*d .. h*d+d-1 of q, k, v, g and of the rows of W_o.
+ *   - "dtype" tensors are float32 when config.dtype == TRI_ATTN_F32 and bf16
+ *     (raw 16-bit patterns) when config.dtype == TRI_ATTN_BF16.
+ *   - Calls validate their arguments on the host first; a validation error
+ *     is returned synchronously and nothing is launched.
+ *   - tri_attn_forward is asynchronous on the given stream (a cudaStream_t
+ *     passed as void*, NULL = legacy default stream).  Errors raised on the
+ *     device (a bounded wait that gave up) are latched in a device status
+ *     word that tri_attn_status_sync reads.
+ *   - A context may be used by one host thread at a time.
+ */
+#ifndef TRI_ATTN_H
+#define TRI_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TRI_ATTN_OK = 0,
+    TRI_ATTN_EINVAL = 1,        /* NULL / out-of-range / misaligned / aliasing argument  */
+    TRI_ATTN_EUNSUPPORTED = 2,  /* shape or dtype the library has no kernel for          */
+    TRI_ATTN_ENOMEM = 3,        /* workspace too small, or host allocation failed        */
+    TRI_ATTN_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed           */
+    TRI_ATTN_ETIMEOUT = 5       /* a device-side bounded wait gave up (status word set)  */
+} tri_attn_status;
+
+typedef enum { TRI_ATTN_STARTING = 0, TRI_ATTN_ENDING = 1 } tri_attn_node;
+typedef enum { TRI_ATTN_F32 = 0, TRI_ATTN_BF16 = 1 } tri_attn_dtype;
+
+/* Kernel path a context runs (tri_attn_path). */
+typedef enum {
+    TRI_ATTN_PATH_SIMT = 0,     /* fp32 CUDA-core kernels: any supported shape, f32 or bf16 storage */
+    TRI_ATTN_PATH_SM103 = 1     /* tcgen05/TMEM/TMA kernels: bf16, c_z = 128, H = 4, d = 32           */
+} tri_attn_path_kind;
+
+typedef struct {
+    int   c_z;          /* pair channels; 1..256                                         */
+    int   heads;        /* H; 1..16                                                      */
+    int   head_dim;     /* d; 1..64, H*d <= 256                                          */
+    int   I_max;        /* largest token count forward will accept; 1..16384             */
+    int   dtype;        /* tri_attn_dtype of Z, the projection weights and out           */
+    float ln_eps;       /* LayerNorm epsilon (> 0; 1e-5 is the usual value)              */
+    int   key_chunks;   /* 1 = one pass over the keys; n > 1 = keys processed in n       */
+                        /* sequential chunks merged by log-sum-exp (Design-CP,           */
+                        /* Methodology 1, on one GPU).  Chunk boundaries are multiples   */
+                        /* of 8 tokens: size = round_up(ceil(I / n), 8).  1..64.         */
+    int   force_simt;   /* nonzero: use the SIMT path even where the sm103 path applies  */
+} tri_attn_config;
+
+/* Device pointers to the module parameters.  Sizes with C = heads*head_dim. */
+typedef struct {
+    const float* ln_gamma;  /* [c_z] fp32                    */
+    const float* ln_beta;   /* [c_z] fp32                    */
+    const void*  w_q;       /* [c_z, C] dtype                */
+    const void*  w_k;       /* [c_z, C] dtype                */
+    const void*  w_v;       /* [c_z, C] dtype                */
+    const void*  w_g;       /* [c_z, C] dtype                */
+    const void*  w_b;       /* [c_z, H] dtype                */
+    const float* b_g;       /* [C] fp32                      */
+    const void*  w_o;       /* [C, c_z] dtype                */
+    const float* b_o;       /* [c_z] fp32, or NULL for zero  */
+} tri_attn_weights;
+
+typedef struct tri_attn_ctx tri_attn_ctx;
+
+/* Create a context for one configuration on the current CUDA device.
+ * Owns host state and one small device allocation (the status word).
+ * Returns EINVAL for a NULL argument or out-of-range field, EUNSUPPORTED when
+ * no kernel covers the shape, ECUDA when the device is not usable.  On error
+ * *out is set to NULL. */
+tri_attn_status tri_attn_create(const tri_attn_config* cfg, tri_attn_ctx** out);
+
+/* Release a context (NULL is a no-op).  Call after the stream work that
+ * uses it has completed. */
+void tri_attn_destroy(tri_attn_ctx* ctx);
+
+/* Path the context runs (tri_attn_path_kind), or -1 for a NULL context. */
+int tri_attn_path(const tri_attn_ctx* ctx);
+
+/* Bytes of device workspace tri_attn_forward needs for I tokens (0 for an
+ * invalid I or a NULL context).  The caller allocates it, 256-byte aligned,
+ * and must not touch it while a forward that uses it is in flight. */
+size_t tri_attn_workspace_bytes(const tri_attn_ctx* ctx, int I);
+
+/* One forward pass.
+ *   node        TRI_ATTN_STARTING or TRI_ATTN_ENDING
+ *   I           tokens, 1 <= I <= cfg.I_max
+ *   Z           [I, I, c_z] dtype, row-major, 16-byte aligned
+ *   token_mask  [I] uint8 (nonzero = valid token), or NULL for all valid
+ *   w           module parameters (struct itself is host memory)
+ *   workspace   >= tri_attn_workspace_bytes(ctx, I) bytes, 256-byte aligned
+ *   out         [I, I, c_z] dtype, 16-byte aligned, must not overlap Z or the workspace
+ *   stream      cudaStream_t as void*
+ * Writes out (the update only).  Asynchronous; returns EINVAL / EUNSUPPORTED
+ * / ENOMEM from validation without launching, ECUDA if a launch fails. */
+tri_attn_status tri_attn_forward(tri_attn_ctx* ctx, int node, int I,
+                                 const void* Z, const uint8_t* token_mask,
+                                 const tri_attn_weights* w,
+                                 void* workspace, size_t workspace_bytes,
+                                 void* out, void* stream);
+
+/* Synchronise `stream`, then read and clear the context's device status word.
+ * Returns ETIMEOUT if a kernel gave up a bounded wait since the last call,
+ * ECUDA if the stream reports an error, else OK. */
+tri_attn_status tri_attn_status_sync(tri_attn_ctx* ctx, void* stream);
+
+/* Per-kernel timing.  tri_attn_set_timing(ctx, 1) clears the record list and
+ * turns recording on: every later forward records a CUDA event pair around
+ * each of its kernel launches, on the launching stream (at most 8192 records;
+ * later launches are not recorded).  tri_attn_kernel_times waits for the
+ * recorded events and writes up to `cap` entries: names[k] (static strings)
+ * and ms[k]; it returns the number of records, or -1 if timing is off.
+ * tri_attn_set_timing(ctx, 0) turns recording off and clears the list. */
+tri_attn_status tri_attn_set_timing(tri_attn_ctx* ctx, int on);
+int tri_attn_kernel_times(tri_attn_ctx* ctx, const char** names, float* ms, int cap);
+
+/* Static description of a status code. */
+const char* tri_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TRI_ATTN_H */

@@ -1,0 +1,50 @@
+"""B300-native gated triangle self-attention (starting and ending node).
+
+The computation runs in libtriattn.so (hand-written CUDA for sm_103a, C ABI in
+include/tri_attn.h); this package is its Python binding.  torch provides
+device memory and streams only.
+"""
+from ._binding import (
+    BF16, ENDING, F32, PATH_SIMT, PATH_SM103, STARTING, EXPORTS,
+    TriAttn, TriAttnConfig, TriAttnError, load_library, status_string,
+)
+
+WEIGHT_NAMES = ("ln_gamma", "ln_beta", "w_q", "w_k", "w_v", "w_g", "w_b", "b_g", "w_o", "b_o")
+
+
+class TriangleAttention:
+    """A context plus a cached workspace: out = op(node, Z, mask, weights).
+
+    Z, weights and mask are torch CUDA tensors laid out as tri_attn.h states
+    (bf16 storage as torch.bfloat16 or raw int16 bits).  Returns `out`.
+    """
+
+    def __init__(self, c_z: int, heads: int, head_dim: int, I_max: int, dtype: str = "bf16",
+                 key_chunks: int = 1, ln_eps: float = 1e-5, force_simt: bool = False):
+        self.ctx = TriAttn(TriAttnConfig(c_z, heads, head_dim, I_max, dtype, ln_eps, key_chunks, force_simt))
+        self._ws = None
+
+    @property
+    def path(self) -> int:
+        return self.ctx.path
+
+    def workspace(self, I: int, device):
+        import torch
+        need = self.ctx.workspace_bytes(I)
+        if self._ws is None or self._ws.numel() < need or self._ws.device != device:
+            self._ws = None
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, node, Z, weights: dict, mask=None, out=None, stream=None):
+        import torch
+        I = Z.shape[0]
+        if out is None:
+            out = torch.empty_like(Z)
+        ws = self.workspace(I, Z.device)
+        self.ctx.forward(node, I, Z, mask, weights, ws, out, stream)
+        return out
+
+
+__all__ = ["TriangleAttention", "TriAttn", "TriAttnConfig", "TriAttnError", "load_library", "status_string",
+           "STARTING", "ENDING", "F32", "BF16", "PATH_SIMT", "PATH_SM103", "EXPORTS", "WEIGHT_NAMES"]

@@ -1,0 +1,178 @@
+"""ctypes binding of libtriattn.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; torch is
+used here for device memory and streams (tensors are passed by data_ptr()).
+The binding raises if the shared library is missing: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libtriattn.so")
+
+OK, EINVAL, EUNSUPPORTED, ENOMEM, ECUDA, ETIMEOUT = range(6)
+STARTING, ENDING = 0, 1
+F32, BF16 = 0, 1
+PATH_SIMT, PATH_SM103 = 0, 1
+NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
+
+EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
+           "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
+           "tri_attn_status_string")
+
+
+class TriAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("c_z", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("I_max", ctypes.c_int), ("dtype", ctypes.c_int), ("ln_eps", ctypes.c_float),
+                ("key_chunks", ctypes.c_int), ("force_simt", ctypes.c_int)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("ln_gamma", "ln_beta", "w_q", "w_k", "w_v", "w_g", "w_b", "b_g", "w_o", "b_o")]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises FileNotFoundError if it was not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with "
+                                "`python -m protein_pair_representation_gate_b300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.tri_attn_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(vp)]
+    lib.tri_attn_create.restype = i
+    lib.tri_attn_destroy.argtypes = [vp]
+    lib.tri_attn_destroy.restype = None
+    lib.tri_attn_path.argtypes = [vp]
+    lib.tri_attn_path.restype = i
+    lib.tri_attn_workspace_bytes.argtypes = [vp, i]
+    lib.tri_attn_workspace_bytes.restype = sz
+    lib.tri_attn_forward.argtypes = [vp, i, i, vp, vp, ctypes.POINTER(Weights), vp, sz, vp, vp]
+    lib.tri_attn_forward.restype = i
+    lib.tri_attn_status_sync.argtypes = [vp, vp]
+    lib.tri_attn_status_sync.restype = i
+    lib.tri_attn_set_timing.argtypes = [vp, i]
+    lib.tri_attn_set_timing.restype = i
+    lib.tri_attn_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), i]
+    lib.tri_attn_kernel_times.restype = i
+    lib.tri_attn_status_string.argtypes = [i]
+    lib.tri_attn_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().tri_attn_status_string(status).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+@dataclass
+class TriAttnConfig:
+    c_z: int
+    heads: int
+    head_dim: int
+    I_max: int
+    dtype: str = "bf16"          # "f32" or "bf16"
+    ln_eps: float = 1e-5
+    key_chunks: int = 1
+    force_simt: bool = False
+
+    def to_c(self) -> Config:
+        return Config(self.c_z, self.heads, self.head_dim, self.I_max, BF16 if self.dtype == "bf16" else F32,
+                      self.ln_eps, self.key_chunks, int(self.force_simt))
+
+
+class TriAttn:
+    """One library context (tri_attn_create / tri_attn_destroy)."""
+
+    def __init__(self, cfg: TriAttnConfig):
+        self.lib = load_library()
+        self.cfg = cfg
+        h = ctypes.c_void_p()
+        st = self.lib.tri_attn_create(ctypes.byref(cfg.to_c()), ctypes.byref(h))
+        if st != OK:
+            raise TriAttnError(st, "tri_attn_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self.lib.tri_attn_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    @property
+    def path(self) -> int:
+        return self.lib.tri_attn_path(self._h)
+
+    def workspace_bytes(self, I: int) -> int:
+        return int(self.lib.tri_attn_workspace_bytes(self._h, I))
+
+    def forward(self, node, I: int, Z, mask, weights: dict, workspace, out, stream=None,
+                workspace_bytes: int | None = None) -> int:
+        """tri_attn_forward on device tensors (or raw pointers); raises on a non-OK status."""
+        st = self.forward_status(node, I, Z, mask, weights, workspace, out, stream, workspace_bytes)
+        if st != OK:
+            raise TriAttnError(st, "tri_attn_forward")
+        return st
+
+    def forward_status(self, node, I, Z, mask, weights, workspace, out, stream=None, workspace_bytes=None) -> int:
+        w = Weights(*[_ptr(weights.get(n)) for n, _ in Weights._fields_])
+        if workspace_bytes is None:
+            workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+        return self.lib.tri_attn_forward(self._h, NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(w),
+                                         _ptr(workspace), workspace_bytes, _ptr(out), _stream_ptr(stream))
+
+    def status_sync(self, stream=None) -> int:
+        return self.lib.tri_attn_status_sync(self._h, _stream_ptr(stream))
+
+    def set_timing(self, on: bool) -> None:
+        self.lib.tri_attn_set_timing(self._h, int(on))
+
+    def kernel_times(self) -> list[tuple[str, float]]:
+        cap = 8192
+        names = (ctypes.c_char_p * cap)()
+        ms = (ctypes.c_float * cap)()
+        n = self.lib.tri_attn_kernel_times(self._h, names, ms, cap)
+        if n < 0:
+            return []
+        return [(names[k].decode(), float(ms[k])) for k in range(min(n, cap))]

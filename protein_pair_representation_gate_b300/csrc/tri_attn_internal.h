@@ -1,0 +1,84 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+//
+// Line-major convention used by every kernel after the projection step:
+// a "line" L is the row i (starting node) or the column j (ending node) that
+// one attention problem runs along, and a "position" x indexes the pairs on
+// that line.  The pair that feeds (L, x) is Z[L, x] for the starting node and
+// Z[x, L] for the ending node.  With the projections written in this
+// orientation, and the pair bias written transposed for the ending node
+// (bias'[h, a, b] = b[h, b, a]), the attention kernels are node-agnostic and
+// only the read of Z and the write of out depend on the node.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tri_attn.h"
+
+namespace tri_attn {
+
+constexpr int kTile = 128;          // token padding granule (one MMA tile of keys or queries)
+
+inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
+inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Device status word bits (set by bounded waits that gave up).
+enum : uint32_t {
+    kStatusTimeoutProducer = 1u << 0,
+    kStatusTimeoutMma = 1u << 1,
+    kStatusTimeoutSoftmax = 1u << 2,
+    kStatusTimeoutEpilogue = 1u << 3,
+};
+
+// Byte offsets of the workspace regions for one (config, I).  Every region
+// starts on a 256-byte boundary.  Element types: SIMT path fp32 everywhere;
+// sm103 path bf16 for q/k/vT/g/bias and fp32 for the chunk state.
+struct Workspace {
+    int I = 0, I_pad = 0;
+    size_t q = 0, k = 0, v = 0, g = 0, bias = 0, u = 0;   // projections
+    size_t o_run = 0, lse_run = 0;                          // key-chunk state (0 bytes if unchunked)
+    size_t wprep = 0, colsum = 0, betaw = 0, wb32 = 0, wo_t = 0, bo = 0;  // prepared weights (sm103)
+    size_t total = 0;
+};
+
+struct Ctx;  // defined in tri_attn_api.cu
+
+// Arguments of one forward, already validated, in device pointers.
+struct FwdArgs {
+    int node, I, I_pad, c_z, H, d;
+    float eps;
+    const void* Z;
+    const uint8_t* mask;     // may be NULL (all valid)
+    tri_attn_weights w;
+    char* ws;                // workspace base
+    const Workspace* lay;
+    void* out;
+    int key_chunks;
+    uint32_t* status;        // device status word
+};
+
+// Records an event pair around a launch when timing is on.
+struct LaunchTimer {
+    virtual void begin(const char* name, cudaStream_t s) = 0;
+    virtual void end(cudaStream_t s) = 0;
+    virtual ~LaunchTimer() {}
+};
+
+// SIMT path (any dtype/shape within the config limits).
+Workspace simt_layout(int I, int c_z, int H, int d, int key_chunks);
+cudaError_t simt_forward(const FwdArgs& a, int dtype, cudaStream_t s, LaunchTimer* t);
+
+// sm103 path (bf16, c_z = 128, H = 4, d = 32).
+bool sm103_supported(int c_z, int H, int d, int dtype);
+Workspace sm103_layout(int I, int key_chunks);
+cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* t);
+
+// Chunk bounds shared by both paths: size = round_up(ceil(I / n), 8).
+inline int chunk_size(int I, int n) {
+    if (n <= 1) return I;
+    int s = (I + n - 1) / n;
+    return round_up(s, 8);
+}
+
+}  // namespace tri_attn

@@ -126,19 +126,35 @@ def _weight(seed: int, stream: int, rows: int, cols: int, fan_in: int, scale: fl
     return w.astype(np.float32)
 
 
-def make_pair_tensor(wl: Workload) -> np.ndarray:
-    """Z as float32 before the storage cast (N(0,1) plus the optional chain offset)."""
+def make_pair_tensor(wl: Workload, threads: int | None = None) -> np.ndarray:
+    """Z as float32 before the storage cast (N(0,1) plus the optional chain offset).
+
+    Row blocks are generated on a thread pool (numpy releases the GIL); every
+    element is a pure function of (seed, stream, index), so the result does
+    not depend on the thread count.
+    """
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
     I, c = wl.I, wl.c_z
     z = np.empty(I * I * c, dtype=np.float32)
-    # generate row blocks to bound the float64 temporary
-    rows_per = max(1, (1 << 24) // (I * c))
-    tmp = np.empty(rows_per * I * c, dtype=np.float64)
-    from .rng import stream_state, splitmix64_outputs  # noqa: F401  (documented generator)
-    for r0 in range(0, I, rows_per):
-        r1 = min(I, r0 + rows_per)
+    rows_per = max(1, (1 << 21) // (I * c))
+    blocks = [(r0, min(I, r0 + rows_per)) for r0 in range(0, I, rows_per)]
+
+    def fill(b):
+        r0, r1 = b
         n = (r1 - r0) * I * c
-        _normal_slice(wl.seed, STREAM_Z, r0 * I * c, n, tmp[:n])
-        z[r0 * I * c: r1 * I * c] = tmp[:n]
+        tmp = np.empty(n, dtype=np.float64)
+        _normal_slice(wl.seed, STREAM_Z, r0 * I * c, n, tmp)
+        z[r0 * I * c: r1 * I * c] = tmp
+
+    nthreads = threads or min(32, os.cpu_count() or 1)
+    if nthreads <= 1 or len(blocks) == 1:
+        for b in blocks:
+            fill(b)
+    else:
+        with ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(fill, blocks))
     z = z.reshape(I, I, c)
     if wl.block_offset != 0.0:
         chain = np.arange(I) // wl.chain_len
