@@ -1,11 +1,936 @@
-// sm_103a tensor-core path (tcgen05 / TMEM / TMA).  Placeholder until the
-// kernels land: reports every shape as unsupported so the SIMT path runs.
+// sm_103a tensor-core path of the gated triangle attention (bf16 storage,
+// fp32 accumulation; c_z = 128, H = 4, d = 32).
+//
+// Three kernels per forward (the attention kernel once per key chunk):
+//
+//   sm103_prep      folds LayerNorm's gamma into the projection weights and
+//                   precomputes the per-column constants that let the
+//                   projection GEMM run on the raw pair vectors:
+//                     LN(z) W = rstd * (z (gamma.W) - mu * colsum(gamma.W)) + beta W
+//   sm103_ln_proj   persistent; per tile of 128 pair vectors on one line:
+//                   TMA load of Z (128B swizzle), tcgen05 MMA z x [Wq|Wk|Wv|Wg]
+//                   (M=128, N=2x256, K=128) into TMEM, LayerNorm statistics
+//                   and the pair bias on CUDA cores, epilogue writing
+//                   q (scaled by log2(e)/sqrt(d)), k, v^T, sigmoid gate and the
+//                   log2(e)-scaled pair bias (-inf on masked keys) in bf16.
+//   sm103_attention one CTA per (line, 256 queries); two softmax warpgroups
+//                   (128 queries each) ping-pong on the tensor core:
+//                   S = Q K^T (tcgen05, TMEM), online softmax with the bias
+//                   added from the TMA-staged tile, P (bf16) written back into
+//                   TMEM over S, O += P V (A operand from TMEM), conditional
+//                   rescaling of O, then normalise, gate, and the output
+//                   projection (u W_o, A operand from TMEM) with the pair
+//                   mask, stored in the node's orientation.  The I x I score
+//                   matrix of a line is never materialised.
+//
+// Sources: the operation as stated in tri_attn.h (Dell page, Evoformer
+// paragraph; Intel page, steps 2 and 4: bias term and fusing it into the
+// score contraction); OpenFold-TRT summary, Methodology: bf16 core, fused
+// kernels; Design-CP summary, Methodology 1: key/value pieces with scores
+// formed on the fly and a log-sum-exp merge across key chunks.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <cstdio>
+
+#include "sm103_ptx.cuh"
 #include "tri_attn_internal.h"
 
 namespace tri_attn {
+namespace {
 
-bool sm103_supported(int, int, int, int) { return false; }
-Workspace sm103_layout(int I, int) { Workspace w; w.I = I; w.I_pad = round_up(I, kTile); return w; }
-cudaError_t sm103_forward(const FwdArgs&, cudaStream_t, LaunchTimer*) { return cudaErrorNotSupported; }
+using namespace ptx;
+
+constexpr int CZ = 128;            // pair channels
+constexpr int NH = 4;              // heads
+constexpr int HD = 32;             // head dim
+constexpr int CH = NH * HD;        // 128 gated channels
+constexpr int NPROJ = 4 * CH;      // 512 MMA output columns: q | k | v | g
+constexpr int NCONST = NPROJ + NH; // + pair bias columns
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kQPad = 256;         // token padding of the sm103 workspace (query-tile pair)
+
+__device__ __forceinline__ void set_abort(volatile int* abort, uint32_t* status, uint32_t code) {
+    *abort = 1;
+    atomicOr(status, code);
+}
+
+// =====================================================================================
+// Weight preparation
+// =====================================================================================
+struct PrepArgs {
+    const float *gamma, *beta, *b_o;
+    const __nv_bfloat16 *w_q, *w_k, *w_v, *w_g, *w_b, *w_o;
+    __nv_bfloat16* wprep;   // [512][128]  row n = (gamma . W)[:, n], K-major for the MMA
+    float* colsum;          // [516]       sum_c of the (rounded) gamma.W column
+    float* betaw;           // [516]       sum_c beta_c W[c, n]
+    float* wb32;            // [128][4]    gamma . W_b in fp32
+    __nv_bfloat16* wo_t;    // [128][128]  W_o transposed: row n = W_o[:, n]
+    float* bo;              // [128]
+};
+
+__global__ void __launch_bounds__(128) sm103_prep(PrepArgs a) {
+    __shared__ float red[2][4];
+    const int n = blockIdx.x, c = threadIdx.x;
+    if (n < NCONST) {
+        float wr, bw;
+        if (n < NPROJ) {
+            const int which = n / CH, col = n % CH;
+            const __nv_bfloat16* W = which == 0 ? a.w_q : which == 1 ? a.w_k : which == 2 ? a.w_v : a.w_g;
+            const float wv = __bfloat162float(W[c * CH + col]);
+            const __nv_bfloat16 r = __float2bfloat16_rn(a.gamma[c] * wv);
+            a.wprep[n * CZ + c] = r;
+            wr = __bfloat162float(r);
+            bw = a.beta[c] * wv;
+        } else {
+            const int h = n - NPROJ;
+            const float wv = __bfloat162float(a.w_b[c * NH + h]);
+            wr = a.gamma[c] * wv;
+            a.wb32[c * NH + h] = wr;
+            bw = a.beta[c] * wv;
+        }
+        for (int o = 16; o; o >>= 1) {
+            wr += __shfl_xor_sync(0xffffffffu, wr, o);
+            bw += __shfl_xor_sync(0xffffffffu, bw, o);
+        }
+        if ((c & 31) == 0) {
+            red[0][c >> 5] = wr;
+            red[1][c >> 5] = bw;
+        }
+        __syncthreads();
+        if (c == 0) {
+            a.colsum[n] = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+            a.betaw[n] = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+        }
+    } else {
+        const int row = n - NCONST;           // output channel of W_o
+        a.wo_t[row * CH + c] = a.w_o[c * CZ + row];
+        if (c == 0) a.bo[row] = a.b_o ? a.b_o[row] : 0.f;
+    }
+}
+
+// =====================================================================================
+// LayerNorm + projections
+// =====================================================================================
+struct ProjParams {
+    int node, I, I_pad, ntx, ntiles;
+    float eps;
+    const uint8_t* mask;
+    const float *colsum, *betaw, *wb32, *b_g;
+    __nv_bfloat16 *q, *k, *vt, *g, *bias;
+    uint32_t* status;
+};
+
+namespace k1 {
+constexpr int kThreads = 384;
+constexpr int kW = 0;                        // 4 x 32 KB: [half(qk|vg)][k-half][256 rows][128 B]
+constexpr int kZ = 131072;                   // 2 stages x 32 KB: [k-half][128 rows][128 B]
+constexpr int kConst = kZ + 2 * 32768;       // colsum[516] betaw[516] wb32[512] b_g[128]
+constexpr int kConstBytes = (NCONST * 2 + CZ * NH + CH) * 4;
+constexpr int kBar = kConst + ((kConstBytes + 127) / 128) * 128;
+constexpr int kSmem = kBar + 256 + 1024;     // + alignment slack
+}  // namespace k1
+
+__global__ void __launch_bounds__(k1::kThreads, 1)
+sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__ CUtensorMap mapZe,
+              const __grid_constant__ CUtensorMap mapW, ProjParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    if (*reinterpret_cast<volatile uint32_t*>(p.status) != 0) return;   // an earlier wait gave up: fail fast
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* s_colsum = reinterpret_cast<float*>(sm + k1::kConst);
+    float* s_betaw = s_colsum + NCONST;
+    float* s_wb = s_betaw + NCONST;        // [128][4]
+    float* s_bg = s_wb + CZ * NH;          // [128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k1::kBar);
+    uint64_t* w_full = bars + 0;
+    uint64_t* z_full = bars + 1;      // [2]
+    uint64_t* z_empty = bars + 3;     // [2]
+    uint64_t* acc_full = bars + 5;    // [2] per half
+    uint64_t* acc_empty = bars + 7;   // [2]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10);
+    volatile int* abort = reinterpret_cast<volatile int*>(bars + 11);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < NCONST; i += blockDim.x) {
+        s_colsum[i] = p.colsum[i];
+        s_betaw[i] = p.betaw[i];
+    }
+    for (int i = threadIdx.x; i < CZ * NH; i += blockDim.x) s_wb[i] = p.wb32[i];
+    for (int i = threadIdx.x; i < CH; i += blockDim.x) s_bg[i] = p.b_g[i];
+    if (threadIdx.x == 0) {
+        mbar_init(w_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(z_full + s, 1);
+            mbar_init(z_empty + s, 1 + 8);
+            mbar_init(acc_full + s, 1);
+            mbar_init(acc_empty + s, 4);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&mapZs);
+            prefetch_tmap(&mapZe);
+            prefetch_tmap(&mapW);
+            mbar_arrive_expect_tx(w_full, 4 * 32768);
+            for (int h2 = 0; h2 < 2; ++h2)
+                for (int kh = 0; kh < 2; ++kh)
+                    tma_load_2d(sm + k1::kW + (h2 * 2 + kh) * 32768, &mapW, w_full, kh * 64, h2 * 256);
+            int j = 0;
+            for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++j) {
+                const int s = j & 1;
+                if (!mbar_wait(z_empty + s, ((j >> 1) & 1) ^ 1, abort)) {
+                    set_abort(abort, p.status, kStatusTimeoutProducer);
+                    break;
+                }
+                const int L = t / p.ntx, x0 = (t % p.ntx) * 128;
+                mbar_arrive_expect_tx(z_full + s, 32768);
+                for (int b = 0; b < 2; ++b) {
+                    uint8_t* dst = sm + k1::kZ + s * 32768 + b * 16384;
+                    if (p.node == TRI_ATTN_STARTING)
+                        tma_load_3d(dst, &mapZs, z_full + s, b * 64, x0, L);
+                    else
+                        tma_load_3d(dst, &mapZe, z_full + s, b * 64, L, x0);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 256);
+            bool ok = mbar_wait(w_full, 0, abort);
+            int j = 0;
+            for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x, ++j) {
+                const int s = j & 1;
+                if (!mbar_wait(z_full + s, (j >> 1) & 1, abort)) { ok = false; break; }
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    if (!mbar_wait(acc_empty + h2, (j & 1) ^ 1, abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t zbase = smem_u32(sm + k1::kZ + s * 32768);
+                    const uint32_t wbase = smem_u32(sm + k1::kW + h2 * 2 * 32768);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = sdesc(zbase + (kk >> 2) * 16384 + (kk & 3) * 32, 1024, kSwizzle128);
+                        const uint64_t bd = sdesc(wbase + (kk >> 2) * 32768 + (kk & 3) * 32, 1024, kSwizzle128);
+                        mma_ss(tmem + h2 * 256, ad, bd, idesc, kk > 0);
+                    }
+                    tc_commit(acc_full + h2);
+                }
+                if (!ok) break;
+                tc_commit(z_empty + s);
+            }
+            if (!ok) set_abort(abort, p.status, kStatusTimeoutMma);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue warpgroups
+        const int wg = (warp - 4) >> 2;          // 0: q,k   1: v,g + pair bias
+        const int wq = warp & 3;                 // TMEM lane quarter
+        const int r = wq * 32 + lane;            // row = pair within the tile
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
+        const float qscale = kLog2e * rsqrtf((float)HD);
+        int j = 0;
+        for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++j) {
+            const int s = j & 1;
+            const int L = t / p.ntx, x = (t % p.ntx) * 128 + r;
+            if (!mbar_wait(z_full + s, (j >> 1) & 1, abort)) {
+                set_abort(abort, p.status, kStatusTimeoutEpilogue);
+                break;
+            }
+            // LayerNorm statistics of the raw pair vector (two passes over registers)
+            uint32_t zr[64];
+            const uint8_t* zb = sm + k1::kZ + s * 32768 + r * 128;
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
+                    zr[b * 32 + c * 4 + 0] = v.x;
+                    zr[b * 32 + c * 4 + 1] = v.y;
+                    zr[b * 32 + c * 4 + 2] = v.z;
+                    zr[b * 32 + c * 4 + 3] = v.w;
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(z_empty + s);
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) sum += bf16lo(zr[i]) + bf16hi(zr[i]);
+            const float mu = sum * (1.f / CZ);
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float a0 = bf16lo(zr[i]) - mu, a1 = bf16hi(zr[i]) - mu;
+                ss = fmaf(a0, a0, fmaf(a1, a1, ss));
+            }
+            const float rstd = rsqrtf(ss * (1.f / CZ) + p.eps);
+            const float nmr = -mu * rstd;
+
+            if (wg == 1) {
+                // pair bias on CUDA cores: b_h = rstd * (z . gW_b[:, h] - mu * colsum) + beta W_b
+                float bh[NH] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float4 w0 = *reinterpret_cast<const float4*>(s_wb + (2 * i) * NH);
+                    const float4 w1 = *reinterpret_cast<const float4*>(s_wb + (2 * i + 1) * NH);
+                    const float z0 = bf16lo(zr[i]), z1 = bf16hi(zr[i]);
+                    bh[0] = fmaf(z0, w0.x, fmaf(z1, w1.x, bh[0]));
+                    bh[1] = fmaf(z0, w0.y, fmaf(z1, w1.y, bh[1]));
+                    bh[2] = fmaf(z0, w0.z, fmaf(z1, w1.z, bh[2]));
+                    bh[3] = fmaf(z0, w0.w, fmaf(z1, w1.w, bh[3]));
+                }
+                const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    const float v = (fmaf(bh[h], rstd, nmr * s_colsum[NPROJ + h]) + s_betaw[NPROJ + h]) * kLog2e;
+                    p.bias[((size_t)h * p.I_pad + L) * p.I_pad + x] = __float2bfloat16_rn(valid ? v : -INFINITY);
+                }
+            }
+
+            if (!mbar_wait(acc_full + wg, j & 1, abort)) {
+                set_abort(abort, p.status, kStatusTimeoutEpilogue);
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int cb = 0; cb < 8; ++cb) {
+                uint32_t acc[32];
+                tmem_ld32(tl + cb * 32, acc);
+                tmem_ld_wait();
+                const int n0 = wg * 256 + cb * 32;
+                const int which = n0 / CH, h = (n0 % CH) / HD;
+                uint32_t o[16];
+                if (which == 3) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float v0 = fmaf(__uint_as_float(acc[e]), rstd, nmr * s_colsum[n0 + e]) + s_betaw[n0 + e];
+                        float v1 = fmaf(__uint_as_float(acc[e + 1]), rstd, nmr * s_colsum[n0 + e + 1]) +
+                                   s_betaw[n0 + e + 1];
+                        v0 += s_bg[h * HD + e];
+                        v1 += s_bg[h * HD + e + 1];
+                        v0 = 1.f / (1.f + ex2(-v0 * kLog2e));
+                        v1 = 1.f / (1.f + ex2(-v1 * kLog2e));
+                        o[e >> 1] = pack_bf16(v0, v1);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + h * HD);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                } else {
+                    const float sc = which == 0 ? qscale : 1.f;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float v0 =
+                            (fmaf(__uint_as_float(acc[e]), rstd, nmr * s_colsum[n0 + e]) + s_betaw[n0 + e]) * sc;
+                        const float v1 = (fmaf(__uint_as_float(acc[e + 1]), rstd, nmr * s_colsum[n0 + e + 1]) +
+                                          s_betaw[n0 + e + 1]) * sc;
+                        o[e >> 1] = pack_bf16(v0, v1);
+                    }
+                    const size_t lh = (size_t)L * NH + h;
+                    if (which == 2) {
+                        __nv_bfloat16* dst = p.vt + lh * HD * p.I_pad + x;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            dst[(size_t)e * p.I_pad] = __ushort_as_bfloat16(static_cast<unsigned short>(o[e >> 1] & 0xFFFFu));
+                            dst[(size_t)(e + 1) * p.I_pad] = __ushort_as_bfloat16(static_cast<unsigned short>(o[e >> 1] >> 16));
+                        }
+                    } else {
+                        __nv_bfloat16* base = which == 0 ? p.q : p.k;
+                        uint4* dst = reinterpret_cast<uint4*>(base + (lh * p.I_pad + x) * HD);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + wg);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// =====================================================================================
+// Attention
+// =====================================================================================
+struct AttnParams {
+    int node, I, I_pad, nk, k_begin, k_end, first, last;
+    const uint8_t* mask;
+    const __nv_bfloat16* g;
+    const float* bo;
+    float *o_run, *lse_run;
+    __nv_bfloat16* out;
+    uint32_t* status;
+};
+
+namespace k2 {
+constexpr int kThreads = 320;                // 2 softmax warpgroups + producer warp + MMA warp
+constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64)
+constexpr int kStage = 32768;                // [2 stages] x 80 KB
+constexpr int kStageBytes = 81920;
+constexpr int kSK = 0, kSV = 8192, kSBa = 16384, kSBb = 49152;   // offsets inside a stage
+constexpr int kWo = kStage + 2 * kStageBytes;   // [2 k-halves][128 rows x 128 B] (SW128)
+constexpr int kBar = kWo + 32768;
+constexpr int kSmem = kBar + 256 + 1024;
+// TMEM columns
+__host__ __device__ constexpr uint32_t colS(int g) { return g * 128u; }        // S / P / out accumulator
+__host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 32u; }  // O accumulator
+__host__ __device__ constexpr uint32_t colU(int g) { return 320u + g * 64u; }  // gated u (bf16 pairs)
+}  // namespace k2
+
+__global__ void __launch_bounds__(k2::kThreads, 1)
+sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapWo, AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    if (*reinterpret_cast<volatile uint32_t*>(p.status) != 0) return;   // an earlier wait gave up: fail fast
+    const int L = blockIdx.y;
+    const int xq0 = blockIdx.x * 256;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (p.mask != nullptr && p.mask[L] == 0) {
+        // the whole line is padding: its outputs are zero
+        if (p.last) {
+            const size_t sL = p.node == TRI_ATTN_STARTING ? (size_t)p.I * CZ : CZ;
+            const size_t sX = p.node == TRI_ATTN_STARTING ? CZ : (size_t)p.I * CZ;
+            for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+                const int x = xq0 + i / 16;
+                if (x < p.I)
+                    reinterpret_cast<uint4*>(p.out + L * sL + x * sX)[i % 16] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k2::kBar);
+    uint64_t* q_full = bars + 0;      // [2]
+    uint64_t* q_empty = bars + 2;     // [2]
+    uint64_t* kv_full = bars + 4;     // [2]
+    uint64_t* kv_empty = bars + 6;    // [2]
+    uint64_t* s_full = bars + 8;      // [2] per softmax group
+    uint64_t* p_full = bars + 10;     // [2]
+    uint64_t* u_full = bars + 12;     // [2]
+    uint64_t* o_full = bars + 14;     // [2]
+    uint64_t* w_full = bars + 16;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
+    volatile int* abort = reinterpret_cast<volatile int*>(bars + 18);
+
+    const int NT = NH * p.nk;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(q_full + s, 1);
+            mbar_init(q_empty + s, 1);
+            mbar_init(kv_full + s, 1);
+            mbar_init(kv_empty + s, 1 + 8);
+            mbar_init(s_full + s, 1);
+            mbar_init(p_full + s, 4);
+            mbar_init(u_full + s, 4);
+            mbar_init(o_full + s, 1);
+        }
+        mbar_init(w_full, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&mapQ);
+            prefetch_tmap(&mapK);
+            prefetch_tmap(&mapVt);
+            prefetch_tmap(&mapB);
+            if (p.last) {
+                prefetch_tmap(&mapWo);
+                mbar_arrive_expect_tx(w_full, 32768);
+                tma_load_2d(sm + k2::kWo, &mapWo, w_full, 0, 0);
+                tma_load_2d(sm + k2::kWo + 16384, &mapWo, w_full, 64, 0);
+            }
+            for (int it = 0; it < NT; ++it) {
+                const int h = it / p.nk, t = it % p.nk, st = it & 1;
+                const int lh = L * NH + h;
+                if (t == 0) {
+                    const int qb = h & 1;
+                    if (!mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort)) {
+                        set_abort(abort, p.status, kStatusTimeoutProducer);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(q_full + qb, 16384);
+                    tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
+                    tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
+                }
+                if (!mbar_wait(kv_empty + st, ((it >> 1) & 1) ^ 1, abort)) {
+                    set_abort(abort, p.status, kStatusTimeoutProducer);
+                    break;
+                }
+                const int k0 = p.k_begin + t * 128;
+                uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
+                mbar_arrive_expect_tx(kv_full + st, k2::kStageBytes);
+                tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
+                tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
+                tma_load_2d(sb + k2::kSV + 4096, &mapVt, kv_full + st, k0 + 64, lh * HD);
+                tma_load_2d(sb + k2::kSBa, &mapB, kv_full + st, k0, h * p.I_pad + xq0);
+                tma_load_2d(sb + k2::kSBa + 16384, &mapB, kv_full + st, k0 + 64, h * p.I_pad + xq0);
+                tma_load_2d(sb + k2::kSBb, &mapB, kv_full + st, k0, h * p.I_pad + xq0 + 128);
+                tma_load_2d(sb + k2::kSBb + 16384, &mapB, kv_full + st, k0 + 64, h * p.I_pad + xq0 + 128);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(128, 128);
+            constexpr uint32_t idO = idesc_bf16_f32(128, 32);
+            bool ok = true;
+            auto issue_pv = [&](int g, int itp) {
+                const int st = itp & 1, tp = itp % p.nk;
+                const uint32_t vb = smem_u32(sm + k2::kStage + st * k2::kStageBytes + k2::kSV);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bd = sdesc(vb + (kk >> 2) * 4096 + (kk & 3) * 32, 1024, kSwizzle128);
+                    mma_ts(tmem + k2::colO(g), tmem + k2::colS(g) + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto issue_s = [&](int g, int it, int qb) {
+                const int st = it & 1;
+                const uint32_t qa = smem_u32(sm + k2::kQ + qb * 16384 + g * 8192);
+                const uint32_t kb = smem_u32(sm + k2::kStage + st * k2::kStageBytes + k2::kSK);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_ss(tmem + k2::colS(g), sdesc(qa + kk * 32, 512, kSwizzle64), sdesc(kb + kk * 32, 512, kSwizzle64),
+                           idS, kk > 0);
+            };
+            for (int it = 0; ok && it < NT; ++it) {
+                const int h = it / p.nk, t = it % p.nk, st = it & 1, qb = h & 1;
+                if (t == 0 && !mbar_wait(q_full + qb, (h >> 1) & 1, abort)) { ok = false; break; }
+                if (!mbar_wait(kv_full + st, (it >> 1) & 1, abort)) { ok = false; break; }
+                tc_fence_after();
+                for (int g = 0; g < 2; ++g) {
+                    if (it > 0) {
+                        if (!mbar_wait(p_full + g, (it - 1) & 1, abort)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(g, it - 1);
+                        if (g == 1) tc_commit(kv_empty + ((it - 1) & 1));
+                    }
+                    issue_s(g, it, qb);
+                    tc_commit(s_full + g);
+                }
+                if (ok && t == p.nk - 1) tc_commit(q_empty + qb);
+            }
+            for (int g = 0; ok && g < 2; ++g) {          // drain: last P V of both groups
+                if (!mbar_wait(p_full + g, (NT - 1) & 1, abort)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv(g, NT - 1);
+                if (g == 1) tc_commit(kv_empty + ((NT - 1) & 1));
+                tc_commit(s_full + g);
+            }
+            if (ok && p.last) {                           // output projection: out = u W_o
+                constexpr uint32_t idP = idesc_bf16_f32(128, 128);
+                ok = mbar_wait(w_full, 0, abort);
+                const uint32_t wb = smem_u32(sm + k2::kWo);
+                for (int g = 0; ok && g < 2; ++g) {
+                    if (!mbar_wait(u_full + g, 0, abort)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bd = sdesc(wb + (kk >> 2) * 16384 + (kk & 3) * 32, 1024, kSwizzle128);
+                        mma_ts(tmem + k2::colS(g), tmem + k2::colU(g) + kk * 8, bd, idP, kk > 0);
+                    }
+                    tc_commit(o_full + g);
+                }
+            }
+            if (!ok) set_abort(abort, p.status, kStatusTimeoutMma);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int g = warp >> 2;                  // 0: queries xq0..+127, 1: xq0+128..+255
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const int x = xq0 + g * 128 + r;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t tS = tl + k2::colS(g), tO = tl + k2::colO(g), tU = tl + k2::colU(g);
+        const int sboff = g ? k2::kSBb : k2::kSBa;
+        float m = -1e30f, l = 0.f;
+        bool ok = true;
+        for (int it = 0; it <= NT; ++it) {
+            if (!mbar_wait(s_full + g, it & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            const int h = it / p.nk, t = it % p.nk;
+            if (it > 0 && (t == 0 || it == NT)) {
+                // ---- the previous head is complete: normalise, merge chunks, gate
+                const int hp = h - 1;
+                uint32_t ov[32];
+                tmem_ld32(tO, ov);
+                tmem_ld_wait();
+                float o[HD];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                float lse = l > 0.f ? m + __log2f(l) : -INFINITY;
+#pragma unroll
+                for (int e = 0; e < HD; ++e) o[e] = __uint_as_float(ov[e]) * inv;
+                const size_t srow = ((size_t)(L * NH + hp)) * p.I_pad + x;
+                if (!p.first) {
+                    const float lr = p.lse_run[srow];
+                    const float top = fmaxf(lr, lse);
+                    if (top != -INFINITY) {
+                        const float wr = ex2(lr - top), wc = ex2(lse - top);
+                        const float it_ = 1.f / (wr + wc);
+                        const float4* orun = reinterpret_cast<const float4*>(p.o_run + srow * HD);
+#pragma unroll
+                        for (int e4 = 0; e4 < HD / 4; ++e4) {
+                            const float4 v = orun[e4];
+                            o[4 * e4 + 0] = (wr * v.x + wc * o[4 * e4 + 0]) * it_;
+                            o[4 * e4 + 1] = (wr * v.y + wc * o[4 * e4 + 1]) * it_;
+                            o[4 * e4 + 2] = (wr * v.z + wc * o[4 * e4 + 2]) * it_;
+                            o[4 * e4 + 3] = (wr * v.w + wc * o[4 * e4 + 3]) * it_;
+                        }
+                        lse = top + __log2f(wr + wc);
+                    }
+                }
+                if (!p.last) {
+                    p.lse_run[srow] = lse;
+                    float4* orun = reinterpret_cast<float4*>(p.o_run + srow * HD);
+#pragma unroll
+                    for (int e4 = 0; e4 < HD / 4; ++e4)
+                        orun[e4] = make_float4(o[4 * e4], o[4 * e4 + 1], o[4 * e4 + 2], o[4 * e4 + 3]);
+                } else {
+                    const uint4* gp = reinterpret_cast<const uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + hp * HD);
+                    uint32_t u[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 gv = gp[i];
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int e = 8 * i + 2 * jj;
+                            u[4 * i + jj] = pack_bf16(bf16lo(gw[jj]) * o[e], bf16hi(gw[jj]) * o[e + 1]);
+                        }
+                    }
+                    tmem_st16(tU + hp * 16, u);
+                }
+            }
+            if (it == NT) break;
+
+            // ---- scores of key tile t: S (fp32, TMEM) + bias (bf16, smem)
+            const int st = it & 1;
+            if (!mbar_wait(kv_full + st, (it >> 1) & 1, abort)) { ok = false; break; }
+            float s[128];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(tS + cb * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(v[i]);
+            }
+            const uint8_t* bb = sm + k2::kStage + st * k2::kStageBytes + sboff + r * 128;
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(bb + b * 16384 + ((c ^ (r & 7)) << 4));
+                    const int k = b * 64 + c * 8;
+                    s[k + 0] += bf16lo(v.x);
+                    s[k + 1] += bf16hi(v.x);
+                    s[k + 2] += bf16lo(v.y);
+                    s[k + 3] += bf16hi(v.y);
+                    s[k + 4] += bf16lo(v.z);
+                    s[k + 5] += bf16hi(v.z);
+                    s[k + 6] += bf16lo(v.w);
+                    s[k + 7] += bf16hi(v.w);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(kv_empty + st);
+            const int k0 = p.k_begin + t * 128;
+            if (k0 + 128 > p.k_end) {                    // ragged last tile of the key range
+                const int nvalid = p.k_end - k0;
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (k >= nvalid) s[k] = -INFINITY;
+            }
+            float mt = s[0];
+#pragma unroll
+            for (int k = 1; k < 128; ++k) mt = fmaxf(mt, s[k]);
+            if (t == 0) {
+                m = fmaxf(mt, -1e30f);
+                l = 0.f;
+            } else {
+                const bool need = mt > m + 8.f;          // rescale only when the max grew by > 2^8
+                if (__any_sync(0xffffffffu, need)) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO, ov);
+                    tmem_ld_wait();
+                    const float mn = need ? mt : m;
+                    const float alpha = ex2(m - mn);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    tmem_st32(tO, ov);
+                    l *= alpha;
+                    m = mn;
+                }
+            }
+            float rs = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int k = 0; k < 128; k += 2) {
+                const float p0 = ex2(s[k] - m), p1 = ex2(s[k + 1] - m);
+                rs += p0 + p1;
+                pk[k >> 1] = pack_bf16(p0, p1);
+            }
+            l += rs;
+            tmem_st32(tS, pk);
+            tmem_st32(tS + 32, pk + 32);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full + g);
+        }
+        if (!ok) set_abort(abort, p.status, kStatusTimeoutSoftmax);
+        if (ok && p.last) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(u_full + g);
+            if (mbar_wait(o_full + g, 0, abort)) {
+                tc_fence_after();
+                const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
+                const size_t pair = p.node == TRI_ATTN_STARTING ? (size_t)L * p.I + x : (size_t)x * p.I + L;
+                uint4* dst = reinterpret_cast<uint4*>(p.out + pair * CZ);
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + cb * 32, v);
+                    tmem_ld_wait();
+                    uint32_t o[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float a0 = valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f;
+                        const float a1 = valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f;
+                        o[e >> 1] = pack_bf16(a0, a1);
+                    }
+                    if (x < p.I) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                }
+            } else {
+                set_abort(abort, p.status, kStatusTimeoutEpilogue);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// =====================================================================================
+// Host side
+// =====================================================================================
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+bool map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+           uint32_t box_rows, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+           uint32_t b0, uint32_t b1, uint32_t b2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace
+
+bool sm103_supported(int c_z, int H, int d, int dtype) {
+    return dtype == TRI_ATTN_BF16 && c_z == CZ && H == NH && d == HD;
+}
+
+Workspace sm103_layout(int I, int key_chunks) {
+    Workspace w;
+    w.I = I;
+    w.I_pad = round_up(I, kQPad);
+    const size_t P = (size_t)I * w.I_pad;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    w.wprep = take((size_t)NPROJ * CZ * 2);
+    w.colsum = take(NCONST * 4);
+    w.betaw = take(NCONST * 4);
+    w.wb32 = take(CZ * NH * 4);
+    w.wo_t = take((size_t)CZ * CH * 2);
+    w.bo = take(CZ * 4);
+    w.q = take(P * CH * 2);
+    w.k = take(P * CH * 2);
+    w.v = take(P * CH * 2);
+    w.g = take(P * CH * 2);
+    w.bias = take((size_t)NH * w.I_pad * w.I_pad * 2);
+    if (key_chunks > 1) {
+        w.o_run = take(P * CH * 4);
+        w.lse_run = take(P * NH * 4);
+    }
+    w.total = off;
+    return w;
+}
+
+cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
+    const Workspace& W = *a.lay;
+    char* ws = a.ws;
+    auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+    auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    const int I = a.I, Ip = a.I_pad;
+
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(sm103_ln_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::kSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(sm103_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, k2::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+
+    // ---- weight preparation
+    PrepArgs pa{a.w.ln_gamma, a.w.ln_beta, a.w.b_o,
+                static_cast<const __nv_bfloat16*>(a.w.w_q), static_cast<const __nv_bfloat16*>(a.w.w_k),
+                static_cast<const __nv_bfloat16*>(a.w.w_v), static_cast<const __nv_bfloat16*>(a.w.w_g),
+                static_cast<const __nv_bfloat16*>(a.w.w_b), static_cast<const __nv_bfloat16*>(a.w.w_o),
+                bf(W.wprep), f32(W.colsum), f32(W.betaw), f32(W.wb32), bf(W.wo_t), f32(W.bo)};
+    if (tm) tm->begin("sm103_prep", s);
+    sm103_prep<<<NCONST + CZ, 128, 0, s>>>(pa);
+    if (tm) tm->end(s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // ---- LayerNorm + projections
+    CUtensorMap mZs, mZe, mW;
+    const uint64_t zrow = (uint64_t)CZ * 2, zline = (uint64_t)I * CZ * 2;
+    if (!map3d(&mZs, a.Z, CZ, I, I, zrow, zline, 64, 128, 1) || !map3d(&mZe, a.Z, CZ, I, I, zrow, zline, 64, 1, 128) ||
+        !map2d(&mW, bf(W.wprep), CZ, NPROJ, CZ * 2, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    ProjParams pp;
+    pp.node = a.node;
+    pp.I = I;
+    pp.I_pad = Ip;
+    pp.ntx = Ip / 128;
+    pp.ntiles = I * pp.ntx;
+    pp.eps = a.eps;
+    pp.mask = a.mask;
+    pp.colsum = f32(W.colsum);
+    pp.betaw = f32(W.betaw);
+    pp.wb32 = f32(W.wb32);
+    pp.b_g = a.w.b_g;
+    pp.q = bf(W.q);
+    pp.k = bf(W.k);
+    pp.vt = bf(W.v);
+    pp.g = bf(W.g);
+    pp.bias = bf(W.bias);
+    pp.status = a.status;
+    {
+        const int grid = pp.ntiles < num_sms() ? pp.ntiles : num_sms();
+        if (tm) tm->begin("sm103_ln_proj", s);
+        sm103_ln_proj<<<grid, k1::kThreads, k1::kSmem, s>>>(mZs, mZe, mW, pp);
+        if (tm) tm->end(s);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    // ---- attention (+ gate, output projection), once per key chunk
+    CUtensorMap mQ, mK, mV, mB, mWo;
+    const uint64_t rows_qk = (uint64_t)I * NH * Ip;
+    if (!map2d(&mQ, bf(W.q), HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mK, bf(W.k), HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mV, bf(W.v), Ip, (uint64_t)I * NH * HD, (uint64_t)Ip * 2, 64, HD, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&mB, bf(W.bias), Ip, (uint64_t)NH * Ip, (uint64_t)Ip * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&mWo, bf(W.wo_t), CH, CZ, CH * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int cs = chunk_size(I, a.key_chunks);
+    for (int k0 = 0; k0 < I; k0 += cs) {
+        const int k1e = k0 + cs < I ? k0 + cs : I;
+        AttnParams ap;
+        ap.node = a.node;
+        ap.I = I;
+        ap.I_pad = Ip;
+        ap.k_begin = k0;
+        ap.k_end = k1e;
+        ap.nk = (k1e - k0 + 127) / 128;
+        ap.first = k0 == 0;
+        ap.last = k1e == I;
+        ap.mask = a.mask;
+        ap.g = bf(W.g);
+        ap.bo = f32(W.bo);
+        ap.o_run = W.o_run ? f32(W.o_run) : nullptr;
+        ap.lse_run = W.lse_run ? f32(W.lse_run) : nullptr;
+        ap.out = static_cast<__nv_bfloat16*>(a.out);
+        ap.status = a.status;
+        dim3 grid(Ip / 256, I);
+        if (tm) tm->begin("sm103_attention", s);
+        sm103_attention<<<grid, k2::kThreads, k2::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+        if (tm) tm->end(s);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 }  // namespace tri_attn
