@@ -52,6 +52,15 @@ constexpr int NCONST = NPROJ + NH; // + pair bias columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kQPad = 256;         // token padding of the sm103 workspace (query-tile pair)
 
+// Block-uniform read of the device status word (one thread reads, all see the
+// same value), so an early return never splits a block at a later barrier.
+__device__ __forceinline__ bool status_set(const uint32_t* status) {
+    __shared__ int skip;
+    if (threadIdx.x == 0) skip = *reinterpret_cast<const volatile uint32_t*>(status) != 0;
+    __syncthreads();
+    return skip != 0;
+}
+
 __device__ __forceinline__ void set_abort(volatile int* abort, uint32_t* status, uint32_t code) {
     *abort = 1;
     atomicOr(status, code);
@@ -137,7 +146,7 @@ __global__ void __launch_bounds__(k1::kThreads, 1)
 sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__ CUtensorMap mapZe,
               const __grid_constant__ CUtensorMap mapW, ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
-    if (*reinterpret_cast<volatile uint32_t*>(p.status) != 0) return;   // an earlier wait gave up: fail fast
+    if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* s_colsum = reinterpret_cast<float*>(sm + k1::kConst);
     float* s_betaw = s_colsum + NCONST;
@@ -399,7 +408,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapWo, AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
-    if (*reinterpret_cast<volatile uint32_t*>(p.status) != 0) return;   // an earlier wait gave up: fail fast
+    if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     const int L = blockIdx.y;
     const int xq0 = blockIdx.x * 256;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
