@@ -1,0 +1,85 @@
+"""C-ABI contract on a real device: validation errors are synchronous and
+launch nothing (the output buffer keeps its sentinel), status and timing
+entry points, path selection."""
+import pytest
+
+from protein_pair_representation_gate_b300 import _binding as B
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def setup():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from synth import make_inputs
+    from synth.device import inputs_to_device
+    inp = make_inputs("evoformer_256", I=64)
+    t = inputs_to_device(inp, "cuda")
+    ctx = B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "bf16"))
+    ws = torch.empty(ctx.workspace_bytes(64), dtype=torch.uint8, device="cuda")
+    return torch, t, ctx, ws
+
+
+def _sentinel(torch, like):
+    return torch.full_like(like, 7.0)
+
+
+def test_paths_selected():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    assert B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "bf16")).path == B.PATH_SM103
+    assert B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "bf16", force_simt=True)).path == B.PATH_SIMT
+    assert B.TriAttn(B.TriAttnConfig(32, 4, 8, 64, "f32")).path == B.PATH_SIMT
+    assert B.TriAttn(B.TriAttnConfig(64, 2, 16, 64, "bf16")).path == B.PATH_SIMT
+    with pytest.raises(B.TriAttnError) as e:
+        B.TriAttn(B.TriAttnConfig(64, 2, 24, 64, "bf16"))
+    assert e.value.status == B.EUNSUPPORTED
+
+
+def test_validation_launches_nothing(setup):
+    torch, t, ctx, ws = setup
+    Z = t["Z"]
+    out = _sentinel(torch, Z)
+    before = out.clone()
+    nbytes = ws.numel()
+    cases = [
+        dict(node=2),
+        dict(I=0),
+        dict(I=65),
+        dict(Z=Z.data_ptr() + 2),
+        dict(out=out.data_ptr() + 2),
+        dict(workspace=ws.data_ptr() + 16),
+        dict(workspace_bytes=nbytes - 1),
+        dict(out=Z.data_ptr()),
+        dict(out=ws.data_ptr()),
+        dict(weights={**t, "w_q": None}),
+        dict(weights={**t, "w_o": t["w_o"].data_ptr() + 2}),
+    ]
+    want = [B.EINVAL] * 6 + [B.ENOMEM] + [B.EINVAL] * 4
+    for kw, st in zip(cases, want):
+        args = dict(node=0, I=64, Z=Z, mask=t["mask"], weights=t, workspace=ws, out=out, workspace_bytes=nbytes)
+        args.update(kw)
+        got = ctx.forward_status(args["node"], args["I"], args["Z"], args["mask"], args["weights"], args["workspace"],
+                                 args["out"], None, args["workspace_bytes"])
+        assert got == st, (kw, got)
+    torch.cuda.synchronize()
+    assert torch.equal(out, before)
+    assert ctx.status_sync() == B.OK
+
+
+def test_timing_records_each_kernel(setup):
+    torch, t, ctx, ws = setup
+    out = torch.empty_like(t["Z"])
+    ctx.set_timing(True)
+    for node in (0, 1):
+        ctx.forward(node, 64, t["Z"], t["mask"], t, ws, out)
+    times = ctx.kernel_times()
+    ctx.set_timing(False)
+    names = [n for n, _ in times]
+    assert names.count("sm103_attention") == 2 and names.count("sm103_ln_proj") == 2
+    assert all(ms > 0 for _, ms in times)
+    assert ctx.kernel_times() == []
+    assert ctx.status_sync() == B.OK
