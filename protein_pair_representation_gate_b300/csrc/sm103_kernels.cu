@@ -141,7 +141,7 @@ struct ProjParams {
 };
 
 namespace k1 {
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;                // 2 epilogue warpgroups + producer warp + MMA warp
 constexpr int kW = 0;                        // 4 x 32 KB: [half(qk|vg)][k-half][256 rows][128 B]
 constexpr int kZ = 131072;                   // 2 stages x 32 KB: [k-half][128 rows][128 B]
 constexpr int kConst = kZ + 2 * 32768;       // colsum[516] betaw[516] wb32[512] b_g[128]
@@ -150,7 +150,7 @@ constexpr int kBar = kConst + ((kConstBytes + 127) / 128) * 128;
 constexpr int kSmem = kBar + 256 + 1024;     // + alignment slack
 }  // namespace k1
 
-__global__ void __launch_bounds__(k1::kThreads, 1)
+__global__ void __maxnreg__(200)
 sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__ CUtensorMap mapZe,
               const __grid_constant__ CUtensorMap mapW, ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -187,7 +187,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 9) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
@@ -196,7 +196,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&mapZs);
@@ -224,7 +224,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 256);
@@ -251,9 +251,9 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
             }
             if (!ok) set_abort(abort, p.status, kStatusTimeoutMma);
         }
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ epilogue warpgroups
-        const int wg = (warp - 4) >> 2;          // 0: q,k   1: v,g + pair bias
+        const int wg = warp >> 2;                // 0: q,k   1: v,g + pair bias
         const int wq = warp & 3;                 // TMEM lane quarter
         const int r = wq * 32 + lane;            // row = pair within the tile
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
@@ -266,48 +266,48 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 set_abort(abort, p.status, kStatusTimeoutEpilogue);
                 break;
             }
-            // LayerNorm statistics of the raw pair vector (two passes over registers)
-            uint32_t zr[64];
+            // LayerNorm statistics of the raw pair vector in one pass over its SMEM row,
+            // shifted by its first channel (exact algebra; avoids cancellation when
+            // the mean is large against the spread).  The pair-bias group also
+            // accumulates z . (gamma W_b)[:, h] for its four heads in the same pass.
             const uint8_t* zb = sm + k1::kZ + s * 32768 + r * 128;
+            const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(zb + ((0 ^ (r & 7)) << 4)));
+            float sd = 0.f, sq = 0.f;
+            float bh0 = 0.f, bh1 = 0.f, bh2 = 0.f, bh3 = 0.f;
+#pragma unroll 2
+            for (int cc = 0; cc < 16; ++cc) {
+                const int b = cc >> 3, c = cc & 7;
+                const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
-                    zr[b * 32 + c * 4 + 0] = v.x;
-                    zr[b * 32 + c * 4 + 1] = v.y;
-                    zr[b * 32 + c * 4 + 2] = v.z;
-                    zr[b * 32 + c * 4 + 3] = v.w;
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    const float z0 = bf16lo(w4[q2]), z1 = bf16hi(w4[q2]);
+                    const float d0 = z0 - shift, d1 = z1 - shift;
+                    sd += d0 + d1;
+                    sq = fmaf(d0, d0, fmaf(d1, d1, sq));
+                    if (wg == 1) {
+                        const int ch = cc * 8 + q2 * 2;
+                        const float4 w0 = *reinterpret_cast<const float4*>(s_wb + ch * NH);
+                        const float4 w1 = *reinterpret_cast<const float4*>(s_wb + (ch + 1) * NH);
+                        bh0 = fmaf(z0, w0.x, fmaf(z1, w1.x, bh0));
+                        bh1 = fmaf(z0, w0.y, fmaf(z1, w1.y, bh1));
+                        bh2 = fmaf(z0, w0.z, fmaf(z1, w1.z, bh2));
+                        bh3 = fmaf(z0, w0.w, fmaf(z1, w1.w, bh3));
+                    }
                 }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(z_empty + s);
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) sum += bf16lo(zr[i]) + bf16hi(zr[i]);
-            const float mu = sum * (1.f / CZ);
-            float ss = 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float a0 = bf16lo(zr[i]) - mu, a1 = bf16hi(zr[i]) - mu;
-                ss = fmaf(a0, a0, fmaf(a1, a1, ss));
-            }
-            const float rstd = rsqrtf(ss * (1.f / CZ) + p.eps);
+            const float md = sd * (1.f / CZ);
+            const float mu = shift + md;
+            const float var = fmaxf(sq * (1.f / CZ) - md * md, 0.f);
+            const float rstd = rsqrtf(var + p.eps);
             const float nmr = -mu * rstd;
 
             if (wg == 1) {
-                // pair bias on CUDA cores: b_h = rstd * (z . gW_b[:, h] - mu * colsum) + beta W_b
-                float bh[NH] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float4 w0 = *reinterpret_cast<const float4*>(s_wb + (2 * i) * NH);
-                    const float4 w1 = *reinterpret_cast<const float4*>(s_wb + (2 * i + 1) * NH);
-                    const float z0 = bf16lo(zr[i]), z1 = bf16hi(zr[i]);
-                    bh[0] = fmaf(z0, w0.x, fmaf(z1, w1.x, bh[0]));
-                    bh[1] = fmaf(z0, w0.y, fmaf(z1, w1.y, bh[1]));
-                    bh[2] = fmaf(z0, w0.z, fmaf(z1, w1.z, bh[2]));
-                    bh[3] = fmaf(z0, w0.w, fmaf(z1, w1.w, bh[3]));
-                }
+                // pair bias: b_h = rstd * (z . gW_b[:, h] - mu * colsum) + beta W_b, in log2 units
                 const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
+                const float bh[NH] = {bh0, bh1, bh2, bh3};
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     const float v = (fmaf(bh[h], rstd, nmr * s_colsum[NPROJ + h]) + s_betaw[NPROJ + h]) * kLog2e;
@@ -320,11 +320,8 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 break;
             }
             tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < 8; ++cb) {
-                uint32_t acc[32];
-                tmem_ld32(tl + cb * 32, acc);
-                tmem_ld_wait();
+            // 32 accumulator columns -> normalised, transformed f16 values -> global
+            auto emit = [&](int cb, const uint32_t (&acc)[32]) {
                 const int n0 = wg * 256 + cb * 32;
                 const int which = n0 / CH, h = (n0 % CH) / HD;
                 uint32_t o[16];
@@ -345,12 +342,12 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                 } else {
                     const float sc = which == 0 ? qscale : 1.f;
+                    const float r2 = rstd * sc, n2 = nmr * sc;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float v0 =
-                            (fmaf(__uint_as_float(acc[e]), rstd, nmr * s_colsum[n0 + e]) + s_betaw[n0 + e]) * sc;
-                        const float v1 = (fmaf(__uint_as_float(acc[e + 1]), rstd, nmr * s_colsum[n0 + e + 1]) +
-                                          s_betaw[n0 + e + 1]) * sc;
+                        const float v0 = fmaf(__uint_as_float(acc[e]), r2, fmaf(n2, s_colsum[n0 + e], s_betaw[n0 + e] * sc));
+                        const float v1 = fmaf(__uint_as_float(acc[e + 1]), r2,
+                                              fmaf(n2, s_colsum[n0 + e + 1], s_betaw[n0 + e + 1] * sc));
                         o[e >> 1] = pack_f16(v0, v1);
                     }
                     const size_t lh = (size_t)L * NH + h;
@@ -369,6 +366,15 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                             dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                     }
                 }
+            };
+#pragma unroll 1
+            for (int cb = 0; cb < 8; cb += 2) {          // two TMEM loads in flight per wait
+                uint32_t acc0[32], acc1[32];
+                tmem_ld32(tl + cb * 32, acc0);
+                tmem_ld32(tl + cb * 32 + 32, acc1);
+                tmem_ld_wait();
+                emit(cb, acc0);
+                emit(cb + 1, acc1);
             }
             tc_fence_before();
             __syncwarp();
@@ -377,7 +383,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -398,20 +404,24 @@ struct AttnParams {
 
 namespace k2 {
 constexpr int kThreads = 320;                // 2 softmax warpgroups + producer warp + MMA warp
-constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64)
-constexpr int kStage = 32768;                // [2 stages] x 80 KB
-constexpr int kStageBytes = 81920;
-constexpr int kSK = 0, kSV = 8192, kSBa = 16384, kSBb = 49152;   // offsets inside a stage
-constexpr int kWo = kStage + 2 * kStageBytes;   // [2 k-halves][128 rows x 128 B] (SW128)
-constexpr int kBar = kWo + 32768;
+constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64); W_o at the end
+constexpr int kStage = 32768;                // [2 stages]
+constexpr int kSK = 0;                       // K tile: 128 keys x 64 B (SW64)
+constexpr int kSV = 8192;                    // V' tile: [2 key-halves] x (32 rows V^T + 16 rows [1;0]) x 128 B
+constexpr int kSVHalf = 6144;                // bytes per key-half of V' (48 rows)
+constexpr int kSBa = 20480, kSBb = 53248;    // bias tiles of the two query tiles: [2 key-halves][128 x 128 B]
+constexpr int kStageBytes = 86016;
+constexpr int kStageTx = 8192 + 8192 + 65536;   // bytes the TMA writes per stage
+constexpr int kBar = kStage + 2 * kStageBytes;
 constexpr int kSmem = kBar + 256 + 1024;
 // TMEM columns
 __host__ __device__ constexpr uint32_t colS(int g) { return g * 128u; }        // S / P / out accumulator
-__host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 32u; }  // O accumulator
-__host__ __device__ constexpr uint32_t colU(int g) { return 320u + g * 64u; }  // gated u (f16 pairs)
+__host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 64u; }  // O (32) | row sum l (1)
+__host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  // gated u (f16 pairs)
+constexpr bool kExpF16x2 = true;             // f16x2 exp2 (one MUFU op per two scores)
 }  // namespace k2
 
-__global__ void __launch_bounds__(k2::kThreads, 1)
+__global__ void __maxnreg__(200)
 sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapWo, AttnParams p) {
@@ -449,6 +459,16 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 18);
 
+    // Rows 32..47 of each V' half: a row of ones (gives the softmax row sum as
+    // output column 32 of P V') and 15 zero rows.  Same in every swizzle phase.
+    for (int i = threadIdx.x; i < 2 * 2 * 2048 / 16; i += blockDim.x) {
+        const int blk = i / 128, off = (i % 128) * 16;         // 4 blocks of 2 KB
+        uint8_t* dst = sm + k2::kStage + (blk >> 1) * k2::kStageBytes + k2::kSV + (blk & 1) * k2::kSVHalf + 4096 + off;
+        const uint32_t one2 = off < 128 ? 0x3C003C00u : 0u;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(one2, one2, one2, one2);
+    }
+    fence_proxy_async_smem();
+
     const int NT = NH * p.nk;
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -481,53 +501,56 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             prefetch_tmap(&mapK);
             prefetch_tmap(&mapVt);
             prefetch_tmap(&mapB);
-            if (p.last) {
-                prefetch_tmap(&mapWo);
-                mbar_arrive_expect_tx(w_full, 32768);
-                tma_load_2d(sm + k2::kWo, &mapWo, w_full, 0, 0);
-                tma_load_2d(sm + k2::kWo + 16384, &mapWo, w_full, 64, 0);
-            }
+            bool ok = true;
             for (int it = 0; it < NT; ++it) {
                 const int h = it / p.nk, t = it % p.nk, st = it & 1;
                 const int lh = L * NH + h;
                 if (t == 0) {
                     const int qb = h & 1;
-                    if (!mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort)) {
-                        set_abort(abort, p.status, kStatusTimeoutProducer);
-                        break;
-                    }
+                    if (!mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort)) { ok = false; break; }
                     mbar_arrive_expect_tx(q_full + qb, 16384);
                     tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
                     tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
                 }
-                if (!mbar_wait(kv_empty + st, ((it >> 1) & 1) ^ 1, abort)) {
-                    set_abort(abort, p.status, kStatusTimeoutProducer);
-                    break;
-                }
+                if (!mbar_wait(kv_empty + st, ((it >> 1) & 1) ^ 1, abort)) { ok = false; break; }
                 const int k0 = p.k_begin + t * 128;
                 uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
-                mbar_arrive_expect_tx(kv_full + st, k2::kStageBytes);
+                mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
                 tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
                 tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
-                tma_load_2d(sb + k2::kSV + 4096, &mapVt, kv_full + st, k0 + 64, lh * HD);
+                tma_load_2d(sb + k2::kSV + k2::kSVHalf, &mapVt, kv_full + st, k0 + 64, lh * HD);
                 tma_load_2d(sb + k2::kSBa, &mapB, kv_full + st, k0, h * p.I_pad + xq0);
                 tma_load_2d(sb + k2::kSBa + 16384, &mapB, kv_full + st, k0 + 64, h * p.I_pad + xq0);
                 tma_load_2d(sb + k2::kSBb, &mapB, kv_full + st, k0, h * p.I_pad + xq0 + 128);
                 tma_load_2d(sb + k2::kSBb + 16384, &mapB, kv_full + st, k0 + 64, h * p.I_pad + xq0 + 128);
             }
+            if (ok && p.last) {
+                // W_o^T goes into the Q region once the last S MMAs of both buffers are done
+                for (int b = 0; ok && b < 2; ++b) {
+                    const int hl = (NH - 1) - (((NH - 1) & 1) != b ? 1 : 0);   // last head h with h & 1 == b
+                    ok = mbar_wait(q_empty + b, (hl >> 1) & 1, abort);
+                }
+                if (ok) {
+                    prefetch_tmap(&mapWo);
+                    mbar_arrive_expect_tx(w_full, 32768);
+                    tma_load_2d(sm + k2::kQ, &mapWo, w_full, 0, 0);
+                    tma_load_2d(sm + k2::kQ + 16384, &mapWo, w_full, 64, 0);
+                }
+            }
+            if (!ok) set_abort(abort, p.status, kStatusTimeoutProducer);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_f16_f32(128, 128);
-            constexpr uint32_t idO = idesc_f16_f32(128, 32);
+            constexpr uint32_t idO = idesc_f16_f32(128, 48);
             bool ok = true;
             auto issue_pv = [&](int g, int itp) {
                 const int st = itp & 1, tp = itp % p.nk;
                 const uint32_t vb = smem_u32(sm + k2::kStage + st * k2::kStageBytes + k2::kSV);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = sdesc(vb + (kk >> 2) * 4096 + (kk & 3) * 32, 1024, kSwizzle128);
+                    const uint64_t bd = sdesc(vb + (kk >> 2) * k2::kSVHalf + (kk & 3) * 32, 1024, kSwizzle128);
                     mma_ts(tmem + k2::colO(g), tmem + k2::colS(g) + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
                 }
             };
@@ -557,7 +580,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 }
                 if (ok && t == p.nk - 1) tc_commit(q_empty + qb);
             }
-            for (int g = 0; ok && g < 2; ++g) {          // drain: last P V of both groups
+            for (int g = 0; ok && g < 2; ++g) {          // drain: last P V' of both groups
                 if (!mbar_wait(p_full + g, (NT - 1) & 1, abort)) { ok = false; break; }
                 tc_fence_after();
                 issue_pv(g, NT - 1);
@@ -567,7 +590,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (ok && p.last) {                           // output projection: out = u W_o
                 constexpr uint32_t idP = idesc_f16_f32(128, 128);
                 ok = mbar_wait(w_full, 0, abort);
-                const uint32_t wb = smem_u32(sm + k2::kWo);
+                const uint32_t wb = smem_u32(sm + k2::kQ);
                 for (int g = 0; ok && g < 2; ++g) {
                     if (!mbar_wait(u_full + g, 0, abort)) { ok = false; break; }
                     tc_fence_after();
@@ -590,7 +613,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tS = tl + k2::colS(g), tO = tl + k2::colO(g), tU = tl + k2::colU(g);
         const int sboff = g ? k2::kSBb : k2::kSBa;
-        float m = -1e30f, l = 0.f;
+        float m = -1e30f;                         // running max (log2 units), finite floor
         bool ok = true;
         for (int it = 0; it <= NT; ++it) {
             if (!mbar_wait(s_full + g, it & 1, abort)) { ok = false; break; }
@@ -601,6 +624,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const int hp = h - 1;
                 uint32_t ov[32];
                 tmem_ld32(tO, ov);
+                const float l = __uint_as_float(tmem_ld1(tO + 32));
                 tmem_ld_wait();
                 float o[HD];
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -653,14 +677,19 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             // ---- scores of key tile t: S (fp32, TMEM) + bias (f16, smem)
             const int st = it & 1;
             if (!mbar_wait(kv_full + st, (it >> 1) & 1, abort)) { ok = false; break; }
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            tmem_ld32(tS, v0);
+            tmem_ld32(tS + 32, v1);
+            tmem_ld32(tS + 64, v2);
+            tmem_ld32(tS + 96, v3);
+            tmem_ld_wait();
             float s[128];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t v[32];
-                tmem_ld32(tS + cb * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[cb * 32 + i] = __uint_as_float(v[i]);
+            for (int i = 0; i < 32; ++i) {
+                s[i] = __uint_as_float(v0[i]);
+                s[32 + i] = __uint_as_float(v1[i]);
+                s[64 + i] = __uint_as_float(v2[i]);
+                s[96 + i] = __uint_as_float(v3[i]);
             }
             const uint8_t* bb = sm + k2::kStage + st * k2::kStageBytes + sboff + r * 128;
 #pragma unroll
@@ -669,14 +698,14 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int c = 0; c < 8; ++c) {
                     const uint4 v = *reinterpret_cast<const uint4*>(bb + b * 16384 + ((c ^ (r & 7)) << 4));
                     const int k = b * 64 + c * 8;
-                    s[k + 0] += f16lo(v.x);
-                    s[k + 1] += f16hi(v.x);
-                    s[k + 2] += f16lo(v.y);
-                    s[k + 3] += f16hi(v.y);
-                    s[k + 4] += f16lo(v.z);
-                    s[k + 5] += f16hi(v.z);
-                    s[k + 6] += f16lo(v.w);
-                    s[k + 7] += f16hi(v.w);
+                    s[k + 0] = add_f16lo(v.x, s[k + 0]);
+                    s[k + 1] = add_f16hi(v.x, s[k + 1]);
+                    s[k + 2] = add_f16lo(v.y, s[k + 2]);
+                    s[k + 3] = add_f16hi(v.y, s[k + 3]);
+                    s[k + 4] = add_f16lo(v.z, s[k + 4]);
+                    s[k + 5] = add_f16hi(v.z, s[k + 5]);
+                    s[k + 6] = add_f16lo(v.w, s[k + 6]);
+                    s[k + 7] = add_f16hi(v.w, s[k + 7]);
                 }
             __syncwarp();
             if (lane == 0) mbar_arrive(kv_empty + st);
@@ -687,36 +716,40 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int k = 0; k < 128; ++k)
                     if (k >= nvalid) s[k] = -INFINITY;
             }
-            float mt = s[0];
+            // tile max: four independent 3-input max chains
+            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
 #pragma unroll
-            for (int k = 1; k < 128; ++k) mt = fmaxf(mt, s[k]);
+            for (int k = 4; k < 128; k += 8) {
+                m0 = max3(m0, s[k], s[k + 1]);
+                m1 = max3(m1, s[k + 2], s[k + 3]);
+                m2 = max3(m2, s[k + 4], s[k + 5]);
+                m3 = max3(m3, s[k + 6], s[k + 7]);
+            }
+            const float mt = fmaxf(max3(m0, m1, m2), m3);
             if (t == 0) {
                 m = fmaxf(mt, -1e30f);
-                l = 0.f;
             } else {
                 const bool need = mt > m + 8.f;          // rescale only when the max grew by > 2^8
                 if (__any_sync(0xffffffffu, need)) {
                     uint32_t ov[32];
                     tmem_ld32(tO, ov);
+                    uint32_t lv = tmem_ld1(tO + 32);
                     tmem_ld_wait();
                     const float mn = need ? mt : m;
                     const float alpha = ex2(m - mn);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                    lv = __float_as_uint(__uint_as_float(lv) * alpha);
                     tmem_st32(tO, ov);
-                    l *= alpha;
+                    tmem_st1(tO + 32, lv);
                     m = mn;
                 }
             }
-            float rs = 0.f;
+            const float negm = -m;
             uint32_t pk[64];
 #pragma unroll
-            for (int k = 0; k < 128; k += 2) {
-                const float p0 = ex2(s[k] - m), p1 = ex2(s[k + 1] - m);
-                rs += p0 + p1;
-                pk[k >> 1] = pack_f16(p0, p1);
-            }
-            l += rs;
+            for (int k = 0; k < 128; k += 2)
+                pk[k >> 1] = k2::kExpF16x2 ? exp2_pair_f16x2(s[k], s[k + 1], negm) : exp2_pair_f32(s[k], s[k + 1], negm);
             tmem_st32(tS, pk);
             tmem_st32(tS + 32, pk + 32);
             tmem_st_wait();

@@ -166,6 +166,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
@@ -214,6 +222,48 @@ __device__ __forceinline__ float f16hi(uint32_t w) {
     float f;
     asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, b;\n\t}" : "=f"(f) : "r"(w));
     return f;
+}
+// x + (f16 half of w), the half converted exactly; one mixed-precision add
+__device__ __forceinline__ float add_f16lo(uint32_t w, float x) {
+    float r;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tadd.f32.f16 %0, a, %2;\n\t}" : "=f"(r) : "r"(w), "f"(x));
+    return r;
+}
+__device__ __forceinline__ float add_f16hi(uint32_t w, float x) {
+    float r;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tadd.f32.f16 %0, b, %2;\n\t}" : "=f"(r) : "r"(w), "f"(x));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// f16x2 (2^(a - m), 2^(b - m)): packed f32x2 subtract, round to f16x2, f16x2 exp2
+__device__ __forceinline__ uint32_t exp2_pair_f16x2(float a, float b, float negm) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 x, y, n;\n\t.reg .f32 lo, hi;\n\t.reg .b32 h;\n\t"
+        "mov.b64 x, {%1, %2};\n\tmov.b64 n, {%3, %3};\n\t"
+        "add.rn.f32x2 y, x, n;\n\tmov.b64 {lo, hi}, y;\n\t"
+        "cvt.rn.f16x2.f32 h, hi, lo;\n\tex2.approx.f16x2 %0, h;\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(negm));
+    return r;
+}
+// same with two f32 exp2 and a rounding pack (more accurate, twice the MUFU work)
+__device__ __forceinline__ uint32_t exp2_pair_f32(float a, float b, float negm) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 x, y, n;\n\t.reg .f32 lo, hi, elo, ehi;\n\t"
+        "mov.b64 x, {%1, %2};\n\tmov.b64 n, {%3, %3};\n\t"
+        "add.rn.f32x2 y, x, n;\n\tmov.b64 {lo, hi}, y;\n\t"
+        "ex2.approx.ftz.f32 elo, lo;\n\tex2.approx.ftz.f32 ehi, hi;\n\t"
+        "cvt.rn.f16x2.f32 %0, ehi, elo;\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(negm));
+    return r;
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
