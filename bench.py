@@ -108,40 +108,62 @@ def dist_setup(args):
     return world, rank, local
 
 
-def cpu_baseline(wl_name: str, budget_s: float = 20.0):
-    """The fp64 oracle on the host cores on a bounded sample: the pair bias over
-    all pairs plus a few starting- and ending-node lines; the full forward time
-    is extrapolated as t_bias + I * t_line for each node."""
-    import numpy as np
-    from oracle import pair_bias, triangle_attention
-    from synth import make_inputs
+class OracleSample:
+    """The fp64 oracle on the host cores, on a bounded sample of one forward step.
 
-    inp = make_inputs(wl_name)
-    wl = inp.workload
-    a = inp.oracle_args()
-    t0 = time.perf_counter()
-    bias = pair_bias(a["Z"], a["ln_gamma"], a["ln_beta"], a["w_b"])
-    t_bias = time.perf_counter() - t0
-    per_line, n_lines = {}, {}
-    rng = np.random.default_rng(0)
-    for node in ("start", "end"):
-        n, t_sum = 0, 0.0
-        while t_sum < budget_s / 2 and n < 32:
-            line = [int(rng.integers(0, wl.I))]
-            t1 = time.perf_counter()
-            triangle_attention(node, a["Z"], a["mask"], a, lines=line, bias=bias)
-            t_sum += time.perf_counter() - t1
-            n += 1
-        per_line[node] = t_sum / n
-        n_lines[node] = n
-    t_step = sum(t_bias + wl.I * per_line[node] for node in ("start", "end"))
-    flops = 2 * wl.attention_flops()
-    threads = _blas_threads()
-    return {"value": flops / t_step / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": (f"fp64 numpy oracle on {wl_name}: pair bias over all {wl.I}x{wl.I} pairs "
-                       f"({t_bias:.1f} s) + {n_lines['start']} starting-node rows and {n_lines['end']} "
-                       f"ending-node columns; step time extrapolated as 2*t_bias + I*(t_row + t_col) = "
-                       f"{t_step:.0f} s")}
+    A step is a starting- and an ending-node forward; the oracle computes the
+    pair bias over all I x I pairs once per node and then each line (row for
+    the starting node, column for the ending node) independently.  The full
+    pair-bias pass is timed once; each sample then times `lines` random rows
+    and columns, and the step time is extrapolated as
+    2 * t_bias + I * (t_row + t_col)."""
+
+    def __init__(self, wl_name: str):
+        from oracle import pair_bias
+        from synth import make_inputs
+
+        self.inp = make_inputs(wl_name)
+        self.wl = self.inp.workload
+        self.a = self.inp.oracle_args()
+        t0 = time.perf_counter()
+        self.bias = pair_bias(self.a["Z"], self.a["ln_gamma"], self.a["ln_beta"], self.a["w_b"])
+        self.t_bias = time.perf_counter() - t0
+        self.calls = 0
+
+    def step(self, lines: int = 2):
+        """One sampled step: returns (extrapolated seconds per step, description)."""
+        import numpy as np
+        from oracle import triangle_attention
+
+        rng = np.random.default_rng(self.calls)
+        self.calls += 1
+        per = {}
+        for node in ("start", "end"):
+            t_sum = 0.0
+            for _ in range(lines):
+                line = [int(rng.integers(0, self.wl.I))]
+                t1 = time.perf_counter()
+                triangle_attention(node, self.a["Z"], self.a["mask"], self.a, lines=line, bias=self.bias)
+                t_sum += time.perf_counter() - t1
+            per[node] = t_sum / lines
+        t_step = 2 * self.t_bias + self.wl.I * (per["start"] + per["end"])
+        desc = (f"fp64 numpy oracle, {self.wl.name}: pair bias over all {self.wl.I}x{self.wl.I} pairs timed once "
+                f"({self.t_bias:.1f} s) + {lines} starting-node rows and {lines} ending-node columns "
+                f"({per['start']:.2f} s, {per['end']:.2f} s each); step = 2*t_bias + I*(t_row + t_col) "
+                f"= {t_step:.0f} s, extrapolated")
+        return t_step, desc
+
+
+def cpu_baseline(wl_name: str, samples: int = 4):
+    """cpu_baseline object of the bench line: the oracle as it stands, on a bounded sample."""
+    o = OracleSample(wl_name)
+    times = []
+    for _ in range(samples):
+        t, desc = o.step(lines=2)
+        times.append(t)
+    t_step = statistics.median(times)
+    return {"value": 2 * o.wl.attention_flops() / t_step / 1e12, "unit": UNIT, "cores": _blas_threads(),
+            "kind": "oracle", "sample": desc + f"; median of {samples} samples"}
 
 
 def _blas_threads():
@@ -154,23 +176,29 @@ def _blas_threads():
 
 
 def run_reference(args, world, rank):
+    """Reference arm: the oracle on the host cores (rank 0 only), same metric and config."""
     if rank != 0:
         return
-    from synth.workloads import WORKLOADS
-    wl = WORKLOADS[args.workload]
     t0 = time.perf_counter()
-    vals = []
+    o = OracleSample(args.workload)
+    wl = o.wl
+    for _ in range(args.warmup and 1):
+        o.step(lines=1)
+    times, desc = [], ""
     for _ in range(max(1, args.steps)):
-        cb = cpu_baseline(args.workload, budget_s=4.0)
-        vals.append(cb["value"])
-    value = statistics.median(vals)
-    cb["value"] = value
+        t, desc = o.step(lines=1)
+        times.append(t)
+    t_step = statistics.median(times)
+    value = 2 * wl.attention_flops() / t_step / 1e12
+    cb = {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+          "sample": desc + f"; median of {len(times)} sampled steps"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": 0, "ms_per_step": 2 * wl.attention_flops() / value / 1e9,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64/Box-Muller), same inputs as the GPU arm",
-            "config": {"workload": args.workload, "I": wl.I, "c_z": wl.c_z, "heads": wl.heads,
-                       "head_dim": wl.head_dim, "nodes": ["start", "end"]},
+            "config": {"workload": f"{args.workload}: I={wl.I}, c_z={wl.c_z}, H={wl.heads}, d={wl.head_dim}, "
+                                   "starting + ending node per step",
+                       "I": wl.I, "c_z": wl.c_z, "heads": wl.heads, "head_dim": wl.head_dim},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0}

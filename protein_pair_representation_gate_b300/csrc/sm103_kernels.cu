@@ -15,7 +15,7 @@
 //                   projection GEMM run on the raw pair vectors:
 //                     LN(z) W = rstd * (z (gamma.W) - mu * colsum(gamma.W)) + beta W
 //   sm103_ln_proj   persistent; per tile of 128 pair vectors on one line:
-//                   TMA load of Z (128B swizzle), tcgen05 MMA z x [Wq|Wk|Wv|Wg]
+//                   TMA load of Z (128B swizzle), tcgen05 MMA z x [Wq|Wv|Wk|Wg]
 //                   (M=128, N=2x256, K=128) into TMEM, LayerNorm statistics
 //                   and the pair bias on CUDA cores, epilogue writing
 //                   q (scaled by log2(e)/sqrt(d)), k, v^T, sigmoid gate and the
@@ -55,7 +55,11 @@ constexpr int CZ = 128;            // pair channels
 constexpr int NH = 4;              // heads
 constexpr int HD = 32;             // head dim
 constexpr int CH = NH * HD;        // 128 gated channels
-constexpr int NPROJ = 4 * CH;      // 512 MMA output columns: q | k | v | g
+constexpr int NPROJ = 4 * CH;      // 512 MMA output columns in four groups of 128
+// Order of the groups in the prepared weights and the accumulator: the first
+// 256 columns (q | v) go to epilogue warpgroup 0, the last 256 (k | g, plus the
+// pair bias computed on CUDA cores) to warpgroup 1, which balances their work.
+constexpr int kGroupQ = 0, kGroupV = 1, kGroupK = 2, kGroupG = 3;
 constexpr int NCONST = NPROJ + NH; // + pair bias columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kQPad = 256;         // token padding of the sm103 workspace (query-tile pair)
@@ -94,8 +98,8 @@ __global__ void __launch_bounds__(128) sm103_prep(PrepArgs a) {
     if (n < NCONST) {
         float wr, bw;
         if (n < NPROJ) {
-            const int which = n / CH, col = n % CH;
-            const __nv_bfloat16* W = which == 0 ? a.w_q : which == 1 ? a.w_k : which == 2 ? a.w_v : a.w_g;
+            const int which = n / CH, col = n % CH;   // row groups q | v | k | g (see kGroup*)
+            const __nv_bfloat16* W = which == kGroupQ ? a.w_q : which == kGroupK ? a.w_k : which == kGroupV ? a.w_v : a.w_g;
             const float wv = __bfloat162float(W[c * CH + col]);
             const __nv_bfloat16 r = __float2bfloat16_rn(a.gamma[c] * wv);
             a.wprep[n * CZ + c] = r;
@@ -150,7 +154,7 @@ constexpr int kBar = kConst + ((kConstBytes + 127) / 128) * 128;
 constexpr int kSmem = kBar + 256 + 1024;     // + alignment slack
 }  // namespace k1
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(k1::kThreads, 1)
 sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__ CUtensorMap mapZe,
               const __grid_constant__ CUtensorMap mapW, ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -253,7 +257,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ epilogue warpgroups
-        const int wg = warp >> 2;                // 0: q,k   1: v,g + pair bias
+        const int wg = warp >> 2;                // 0: q, v   1: k, g + pair bias
         const int wq = warp & 3;                 // TMEM lane quarter
         const int r = wq * 32 + lane;            // row = pair within the tile
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
@@ -325,7 +329,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 const int n0 = wg * 256 + cb * 32;
                 const int which = n0 / CH, h = (n0 % CH) / HD;
                 uint32_t o[16];
-                if (which == 3) {
+                if (which == kGroupG) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float v0 = fmaf(__uint_as_float(acc[e]), rstd, nmr * s_colsum[n0 + e]) + s_betaw[n0 + e];
@@ -341,7 +345,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                 } else {
-                    const float sc = which == 0 ? qscale : 1.f;
+                    const float sc = which == kGroupQ ? qscale : 1.f;
                     const float r2 = rstd * sc, n2 = nmr * sc;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -351,7 +355,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                         o[e >> 1] = pack_f16(v0, v1);
                     }
                     const size_t lh = (size_t)L * NH + h;
-                    if (which == 2) {
+                    if (which == kGroupV) {
                         unsigned short* dst = reinterpret_cast<unsigned short*>(p.vt + lh * HD * p.I_pad + x);
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
@@ -359,7 +363,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                             dst[(size_t)(e + 1) * p.I_pad] = static_cast<unsigned short>(o[e >> 1] >> 16);
                         }
                     } else {
-                        __half* base = which == 0 ? p.q : p.k;
+                        __half* base = which == kGroupQ ? p.q : p.k;
                         uint4* dst = reinterpret_cast<uint4*>(base + (lh * p.I_pad + x) * HD);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
@@ -403,7 +407,7 @@ struct AttnParams {
 };
 
 namespace k2 {
-constexpr int kThreads = 320;                // 2 softmax warpgroups + producer warp + MMA warp
+constexpr int kThreads = 384;                // control warpgroup (producer, MMA, 2 idle) + 2 softmax warpgroups
 constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64); W_o at the end
 constexpr int kStage = 32768;                // [2 stages]
 constexpr int kSK = 0;                       // K tile: 128 keys x 64 B (SW64)
@@ -421,7 +425,7 @@ __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  /
 constexpr bool kExpF16x2 = true;             // f16x2 exp2 (one MUFU op per two scores)
 }  // namespace k2
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(k2::kThreads, 1)
 sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapWo, AttnParams p) {
@@ -485,7 +489,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
@@ -494,7 +498,13 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 8) {
+    // Register budget: launched at 168 per thread.  The control warpgroup
+    // (warps 0-3, one warp per SM sub-partition) drops to 56 and each softmax
+    // warp grows to 224, so every sub-partition releases exactly what it takes
+    // (32 x 112 = 2 x 32 x 56 registers) and no increase can wait on another
+    // sub-partition.
+    if (warp == 0) {
+        setmaxnreg_dec<56>();
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&mapQ);
@@ -539,7 +549,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
             if (!ok) set_abort(abort, p.status, kStatusTimeoutProducer);
         }
-    } else if (warp == 9) {
+    } else if (warp == 1) {
+        setmaxnreg_dec<56>();
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = idesc_f16_f32(128, 128);
@@ -604,9 +615,12 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
             if (!ok) set_abort(abort, p.status, kStatusTimeoutMma);
         }
+    } else if (warp < 4) {
+        setmaxnreg_dec<56>();                     // idle warps of the control warpgroup
     } else {
+        setmaxnreg_inc<224>();
         // ------------------------------------------------------------ softmax warpgroups
-        const int g = warp >> 2;                  // 0: queries xq0..+127, 1: xq0+128..+255
+        const int g = (warp - 4) >> 2;            // 0: queries xq0..+127, 1: xq0+128..+255
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
         const int x = xq0 + g * 128 + r;
@@ -677,23 +691,20 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             // ---- scores of key tile t: S (fp32, TMEM) + bias (f16, smem)
             const int st = it & 1;
             if (!mbar_wait(kv_full + st, (it >> 1) & 1, abort)) { ok = false; break; }
-            uint32_t v0[32], v1[32], v2[32], v3[32];
-            tmem_ld32(tS, v0);
-            tmem_ld32(tS + 32, v1);
-            tmem_ld32(tS + 64, v2);
-            tmem_ld32(tS + 96, v3);
-            tmem_ld_wait();
+            // two halves of 64 keys: TMEM load (two loads in flight), then the bias add
             float s[128];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                s[i] = __uint_as_float(v0[i]);
-                s[32 + i] = __uint_as_float(v1[i]);
-                s[64 + i] = __uint_as_float(v2[i]);
-                s[96 + i] = __uint_as_float(v3[i]);
-            }
             const uint8_t* bb = sm + k2::kStage + st * k2::kStageBytes + sboff + r * 128;
 #pragma unroll
-            for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < 2; ++b) {
+                uint32_t va[32], vb[32];
+                tmem_ld32(tS + b * 64, va);
+                tmem_ld32(tS + b * 64 + 32, vb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    s[b * 64 + i] = __uint_as_float(va[i]);
+                    s[b * 64 + 32 + i] = __uint_as_float(vb[i]);
+                }
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 v = *reinterpret_cast<const uint4*>(bb + b * 16384 + ((c ^ (r & 7)) << 4));
@@ -707,6 +718,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     s[k + 6] = add_f16lo(v.w, s[k + 6]);
                     s[k + 7] = add_f16hi(v.w, s[k + 7]);
                 }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(kv_empty + st);
             const int k0 = p.k_begin + t * 128;
@@ -793,7 +805,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
