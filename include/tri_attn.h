@@ -158,6 +158,35 @@ tri_attn_status tri_attn_status_sync(tri_attn_ctx* ctx, void* stream);
 tri_attn_status tri_attn_set_timing(tri_attn_ctx* ctx, int on);
 int tri_attn_kernel_times(tri_attn_ctx* ctx, const char** names, float* ms, int cap);
 
+/* Allocation-free forward, for callers that cannot allocate device memory.
+ *
+ * Some callers have their input and output buffers but may not call
+ * cudaMalloc: code running inside a host callback or a custom allocator, a
+ * plugin whose host runtime owns every device allocation, or a process whose
+ * device memory is fully reserved up front.  They can use neither the
+ * caller-allocated workspace of tri_attn_forward nor tri_attn_create (which
+ * allocates the status word).  This entry point needs neither: its workspace
+ * is a file-scope device array of the library (33.5 MB: the sm103 workspace
+ * at I = 128 plus a status word), which every GPU that loads the library
+ * holds until the process exits.  The paper has no counterpart of it.
+ *
+ *   shape       bf16 Z / weights / out, c_z = 128, H = 4, d = 32, one key chunk
+ *               (the sm103 kernels; sm_103 devices only, else EUNSUPPORTED)
+ *   I           1 <= I <= 128; larger I returns TRI_ATTN_EUNSUPPORTED
+ *   ln_eps      LayerNorm epsilon, 0 < ln_eps <= 1
+ *   other args  as for tri_attn_forward (device pointers, 16-byte aligned;
+ *               out must not overlap Z)
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it: make that first call before any
+ * stream capture.  Every call shares the one array and leaves its contents
+ * behind; the status word inside it is cleared at the start of each call, and
+ * a device-side wait that gives up leaves `out` incomplete without being
+ * reported here.  Calls whose work overlaps on the GPU race on the array:
+ * issue them on one stream, or otherwise order them. */
+tri_attn_status tri_attn_forward_static(int node, int I, const void* Z, const uint8_t* token_mask,
+                                        const tri_attn_weights* w, float ln_eps, void* out, void* stream);
+
 /* Static description of a status code. */
 const char* tri_attn_status_string(int status);
 

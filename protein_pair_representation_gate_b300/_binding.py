@@ -21,7 +21,7 @@ NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
 
 EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
            "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
-           "tri_attn_status_string")
+           "tri_attn_status_string", "tri_attn_forward_static")
 
 
 class TriAttnError(RuntimeError):
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tri_attn_set_timing.restype = i
     lib.tri_attn_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), i]
     lib.tri_attn_kernel_times.restype = i
+    lib.tri_attn_forward_static.argtypes = [i, i, vp, vp, ctypes.POINTER(Weights), ctypes.c_float, vp, vp]
+    lib.tri_attn_forward_static.restype = i
     lib.tri_attn_status_string.argtypes = [i]
     lib.tri_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -111,6 +113,14 @@ class TriAttnConfig:
     def to_c(self) -> Config:
         return Config(self.c_z, self.heads, self.head_dim, self.I_max, BF16 if self.dtype == "bf16" else F32,
                       self.ln_eps, self.key_chunks, int(self.force_simt))
+
+
+def forward_static(node, I: int, Z, mask, weights: dict, out, ln_eps: float = 1e-5, stream=None) -> int:
+    """tri_attn_forward_static (no context, no workspace: library-owned device scratch); returns the status."""
+    lib = load_library()
+    w = Weights(*[_ptr(weights.get(n)) for n, _ in Weights._fields_])
+    return lib.tri_attn_forward_static(NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(w), ln_eps,
+                                       _ptr(out), _stream_ptr(stream))
 
 
 class TriAttn:
