@@ -408,21 +408,22 @@ struct AttnParams {
 
 namespace k2 {
 constexpr int kThreads = 384;                // control warpgroup (producer, MMA, 2 idle) + 2 softmax warpgroups
+constexpr int kKT = 64;                      // keys per stage (one S sub-tile)
+constexpr int kStages = 4;                  // power of two: stage = it & 3, phase = (it >> 2) & 1
 constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64); W_o at the end
-constexpr int kStage = 32768;                // [2 stages]
-constexpr int kSK = 0;                       // K tile: 128 keys x 64 B (SW64)
-constexpr int kSV = 8192;                    // V' tile: [2 key-halves] x (32 rows V^T + 16 rows [1;0]) x 128 B
-constexpr int kSVHalf = 6144;                // bytes per key-half of V' (48 rows)
-constexpr int kSBa = 20480, kSBb = 53248;    // bias tiles of the two query tiles: [2 key-halves][128 x 128 B]
-constexpr int kStageBytes = 86016;
-constexpr int kStageTx = 8192 + 8192 + 65536;   // bytes the TMA writes per stage
-constexpr int kBar = kStage + 2 * kStageBytes;
-constexpr int kSmem = kBar + 256 + 1024;
+constexpr int kStage = 32768;
+constexpr int kSK = 0;                       // K tile: 64 keys x 64 B (SW64)
+constexpr int kSV = 4096;                    // V' tile: 32 rows V^T + 16 rows [1; 0], 128 B each (SW128)
+constexpr int kSBa = 10240, kSBb = 26624;    // bias tiles of the two query tiles: 128 rows x 128 B (SW128)
+constexpr int kStageBytes = 43008;
+constexpr int kStageTx = 4096 + 4096 + 32768;   // bytes the TMA writes per stage
+constexpr int kBar = kStage + kStages * kStageBytes;
+constexpr int kSmem = kBar + 512 + 1024;     // barriers + alignment slack
 // TMEM columns
-__host__ __device__ constexpr uint32_t colS(int g) { return g * 128u; }        // S / P / out accumulator
+__host__ __device__ constexpr uint32_t colS(int g, int b) { return g * 128u + b * 64u; }   // S / P buffers
 __host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 64u; }  // O (32) | row sum l (1)
 __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  // gated u (f16 pairs)
-constexpr bool kExpF16x2 = true;             // f16x2 exp2 (one MUFU op per two scores)
+static_assert(kStages == 4, "stage index and phase are computed with it & 3 and (it >> 2) & 1");
 }  // namespace k2
 
 __global__ void __launch_bounds__(k2::kThreads, 1)
@@ -453,37 +454,45 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k2::kBar);
     uint64_t* q_full = bars + 0;      // [2]
     uint64_t* q_empty = bars + 2;     // [2]
-    uint64_t* kv_full = bars + 4;     // [2]
-    uint64_t* kv_empty = bars + 6;    // [2]
-    uint64_t* s_full = bars + 8;      // [2] per softmax group
-    uint64_t* p_full = bars + 10;     // [2]
-    uint64_t* u_full = bars + 12;     // [2]
-    uint64_t* o_full = bars + 14;     // [2]
-    uint64_t* w_full = bars + 16;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
-    volatile int* abort = reinterpret_cast<volatile int*>(bars + 18);
+    uint64_t* kv_full = bars + 4;     // [4]
+    uint64_t* kv_empty = bars + 8;    // [4]
+    uint64_t* s_full = bars + 12;     // [2 groups][2 buffers]
+    // P and O barriers alternate by tile parity: with two S buffers a softmax group
+    // can write P(it) and P(it+1) before the MMA warp has waited for P(it), and one
+    // barrier would then run two phases ahead of its waiter.
+    uint64_t* p_full = bars + 16;     // [2 groups][tile parity]: P(it) of group g written
+    uint64_t* o_ready = bars + 20;    // [2 groups][tile parity]: P V'(it) of group g done
+    uint64_t* u_full = bars + 24;     // [2]
+    uint64_t* o_full = bars + 26;     // [2]
+    uint64_t* w_full = bars + 28;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 29);
+    volatile int* abort = reinterpret_cast<volatile int*>(bars + 30);
 
-    // Rows 32..47 of each V' half: a row of ones (gives the softmax row sum as
+    // Rows 32..47 of each stage's V': a row of ones (gives the softmax row sum as
     // output column 32 of P V') and 15 zero rows.  Same in every swizzle phase.
-    for (int i = threadIdx.x; i < 2 * 2 * 2048 / 16; i += blockDim.x) {
-        const int blk = i / 128, off = (i % 128) * 16;         // 4 blocks of 2 KB
-        uint8_t* dst = sm + k2::kStage + (blk >> 1) * k2::kStageBytes + k2::kSV + (blk & 1) * k2::kSVHalf + 4096 + off;
+    for (int i = threadIdx.x; i < k2::kStages * 2048 / 16; i += blockDim.x) {
+        const int st = i / 128, off = (i % 128) * 16;
+        uint8_t* dst = sm + k2::kStage + st * k2::kStageBytes + k2::kSV + 4096 + off;
         const uint32_t one2 = off < 128 ? 0x3C003C00u : 0u;
         *reinterpret_cast<uint4*>(dst) = make_uint4(one2, one2, one2, one2);
     }
     fence_proxy_async_smem();
 
-    const int NT = NH * p.nk;
+    const int nk = p.nk;
+    const int NT = NH * nk;
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(q_full + s, 1);
             mbar_init(q_empty + s, 1);
+            mbar_init(u_full + s, 4);
+            mbar_init(o_full + s, 1);
+        }
+        for (int s = 0; s < k2::kStages; ++s) {
             mbar_init(kv_full + s, 1);
             mbar_init(kv_empty + s, 1 + 8);
             mbar_init(s_full + s, 1);
             mbar_init(p_full + s, 4);
-            mbar_init(u_full + s, 4);
-            mbar_init(o_full + s, 1);
+            mbar_init(o_ready + s, 1);
         }
         mbar_init(w_full, 1);
         *abort = 0;
@@ -499,250 +508,310 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const uint32_t tmem = *tmem_holder;
 
     // Register budget: launched at 168 per thread.  The control warpgroup
-    // (warps 0-3, one warp per SM sub-partition) drops to 56 and each softmax
-    // warp grows to 224, so every sub-partition releases exactly what it takes
-    // (32 x 112 = 2 x 32 x 56 registers) and no increase can wait on another
+    // (warps 0-3, one warp per SM sub-partition) drops to 88 and each softmax
+    // warp grows to 208, so every sub-partition releases exactly what it takes
+    // (32 x 80 = 2 x 32 x 40 registers) and no increase can wait on another
     // sub-partition.
+    // The producer and MMA warps run their loops converged (every lane waits on the
+    // same barriers, so loop control and addresses stay warp-uniform) and one
+    // elected lane issues each TMA copy or tcgen05 instruction.
     if (warp == 0) {
-        setmaxnreg_dec<56>();
+        setmaxnreg_dec<88>();
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        const bool leader = elect_one();
+        if (leader) {
             prefetch_tmap(&mapQ);
             prefetch_tmap(&mapK);
             prefetch_tmap(&mapVt);
             prefetch_tmap(&mapB);
-            bool ok = true;
-            for (int it = 0; it < NT; ++it) {
-                const int h = it / p.nk, t = it % p.nk, st = it & 1;
-                const int lh = L * NH + h;
+        }
+        bool ok = true;
+        for (int h = 0, it = 0; ok && h < NH; ++h) {
+            const int lh = L * NH + h;
+            for (int t = 0; t < nk; ++t, ++it) {
+                const int st = it & (k2::kStages - 1);
                 if (t == 0) {
                     const int qb = h & 1;
-                    if (!mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort)) { ok = false; break; }
-                    mbar_arrive_expect_tx(q_full + qb, 16384);
-                    tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
-                    tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
+                    ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort));
+                    if (!ok) break;
+                    if (leader) {
+                        mbar_arrive_expect_tx(q_full + qb, 16384);
+                        tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
+                        tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
+                    }
                 }
-                if (!mbar_wait(kv_empty + st, ((it >> 1) & 1) ^ 1, abort)) { ok = false; break; }
-                const int k0 = p.k_begin + t * 128;
-                uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
-                mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
-                tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
-                tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
-                tma_load_2d(sb + k2::kSV + k2::kSVHalf, &mapVt, kv_full + st, k0 + 64, lh * HD);
-                tma_load_2d(sb + k2::kSBa, &mapB, kv_full + st, k0, h * p.I_pad + xq0);
-                tma_load_2d(sb + k2::kSBa + 16384, &mapB, kv_full + st, k0 + 64, h * p.I_pad + xq0);
-                tma_load_2d(sb + k2::kSBb, &mapB, kv_full + st, k0, h * p.I_pad + xq0 + 128);
-                tma_load_2d(sb + k2::kSBb + 16384, &mapB, kv_full + st, k0 + 64, h * p.I_pad + xq0 + 128);
+                ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it >> 2) & 1) ^ 1, abort));
+                if (!ok) break;
+                if (leader) {
+                    const int k0 = p.k_begin + t * k2::kKT;
+                    uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
+                    mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
+                    tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
+                    tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
+                    tma_load_2d(sb + k2::kSBa, &mapB, kv_full + st, k0, h * p.I_pad + xq0);
+                    tma_load_2d(sb + k2::kSBb, &mapB, kv_full + st, k0, h * p.I_pad + xq0 + 128);
+                }
+                __syncwarp();
             }
-            if (ok && p.last) {
-                // W_o^T goes into the Q region once the last S MMAs of both buffers are done
-                for (int b = 0; ok && b < 2; ++b) {
-                    const int hl = (NH - 1) - (((NH - 1) & 1) != b ? 1 : 0);   // last head h with h & 1 == b
-                    ok = mbar_wait(q_empty + b, (hl >> 1) & 1, abort);
-                }
-                if (ok) {
-                    prefetch_tmap(&mapWo);
-                    mbar_arrive_expect_tx(w_full, 32768);
-                    tma_load_2d(sm + k2::kQ, &mapWo, w_full, 0, 0);
-                    tma_load_2d(sm + k2::kQ + 16384, &mapWo, w_full, 64, 0);
-                }
-            }
-            if (!ok) set_abort(abort, p.status, kStatusTimeoutProducer);
         }
+        if (ok && p.last) {
+            // W_o^T goes into the Q region once the last S MMAs of both buffers are done
+            for (int b = 0; ok && b < 2; ++b) {
+                const int hl = (NH - 1) - (((NH - 1) & 1) != b ? 1 : 0);   // last head h with h & 1 == b
+                ok = __all_sync(0xffffffffu, mbar_wait(q_empty + b, (hl >> 1) & 1, abort));
+            }
+            if (ok && leader) {
+                prefetch_tmap(&mapWo);
+                mbar_arrive_expect_tx(w_full, 32768);
+                tma_load_2d(sm + k2::kQ, &mapWo, w_full, 0, 0);
+                tma_load_2d(sm + k2::kQ + 16384, &mapWo, w_full, 64, 0);
+            }
+        }
+        if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
     } else if (warp == 1) {
-        setmaxnreg_dec<56>();
+        setmaxnreg_dec<88>();
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_f16_f32(128, 128);
-            constexpr uint32_t idO = idesc_f16_f32(128, 48);
-            bool ok = true;
-            auto issue_pv = [&](int g, int itp) {
-                const int st = itp & 1, tp = itp % p.nk;
-                const uint32_t vb = smem_u32(sm + k2::kStage + st * k2::kStageBytes + k2::kSV);
+        const bool leader = elect_one();
+        constexpr uint32_t idS = idesc_f16_f32(128, k2::kKT);
+        constexpr uint32_t idO = idesc_f16_f32(128, 48);
+        constexpr uint64_t tK = sdesc_tmpl(512, kSwizzle64);      // Q and K tiles: 64 B rows
+        constexpr uint64_t tV = sdesc_tmpl(1024, kSwizzle128);    // V' and W_o^T: 128 B rows
+        const uint32_t qbase = smem_u32(sm + k2::kQ), sbase = smem_u32(sm + k2::kStage);
+        // descriptors of stage 0 / Q buffer 0; other stages and buffers are fixed
+        // offsets in the 16-byte address field (no carry: shared addresses < 256 KB)
+        const uint64_t dQ0 = sdesc_at(tK, qbase), dK0 = sdesc_at(tK, sbase + k2::kSK);
+        const uint64_t dV0 = sdesc_at(tV, sbase + k2::kSV);
+        constexpr uint64_t kStageStep = k2::kStageBytes >> 4;
+        bool ok = true;
+        // S_g(it) = Q_g K(it)^T into buffer it & 1 (head parity qb)
+        auto issue_s = [&](int g, int it, int qb) {
+            const uint64_t qa = dQ0 + static_cast<uint64_t>(qb * 1024 + g * 512);
+            const uint64_t kb = dK0 + static_cast<uint64_t>(it & (k2::kStages - 1)) * kStageStep;
+            const uint32_t d = tmem + k2::colS(g, it & 1);
+            mma_ss(d, qa, kb, idS, 0u);
+            mma_ss(d, qa + 2, kb + 2, idS, 1u);
+        };
+        // O_g (+)= P_g(it) V'(it); the first tile of a head (t == 0) overwrites
+        auto issue_pv = [&](int g, int it, int t) {
+            const uint64_t vb = dV0 + static_cast<uint64_t>(it & (k2::kStages - 1)) * kStageStep;
+            const uint32_t a = tmem + k2::colS(g, it & 1), d = tmem + k2::colO(g);
+            const uint32_t first = t > 0 ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = sdesc(vb + (kk >> 2) * k2::kSVHalf + (kk & 3) * 32, 1024, kSwizzle128);
-                    mma_ts(tmem + k2::colO(g), tmem + k2::colS(g) + kk * 8, bd, idO, (tp > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
-            auto issue_s = [&](int g, int it, int qb) {
-                const int st = it & 1;
-                const uint32_t qa = smem_u32(sm + k2::kQ + qb * 16384 + g * 8192);
-                const uint32_t kb = smem_u32(sm + k2::kStage + st * k2::kStageBytes + k2::kSK);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_ss(tmem + k2::colS(g), sdesc(qa + kk * 32, 512, kSwizzle64), sdesc(kb + kk * 32, 512, kSwizzle64),
-                           idS, kk > 0);
-            };
-            for (int it = 0; ok && it < NT; ++it) {
-                const int h = it / p.nk, t = it % p.nk, st = it & 1, qb = h & 1;
-                if (t == 0 && !mbar_wait(q_full + qb, (h >> 1) & 1, abort)) { ok = false; break; }
-                if (!mbar_wait(kv_full + st, (it >> 1) & 1, abort)) { ok = false; break; }
+            for (int kk = 0; kk < k2::kKT / 16; ++kk) mma_ts(d, a + kk * 8, vb + kk * 2, idO, kk > 0 ? 1u : first);
+        };
+        // operands of S(it) present: Q of its head (first tile), K of its stage
+        auto s_ready = [&](int it, int h, int t) -> bool {
+            bool r = true;
+            if (t == 0) r = mbar_wait(q_full + (h & 1), (h >> 1) & 1, abort);
+            if (r) r = mbar_wait(kv_full + (it & (k2::kStages - 1)), (it >> 2) & 1, abort);
+            return __all_sync(0xffffffffu, r);
+        };
+        // prologue: S of tiles 0 and 1
+        int hn = 0, tn = 0;                           // (head, tile) of the next S to issue
+        for (int it = 0; ok && it < 2 && it < NT; ++it) {
+            ok = s_ready(it, hn, tn);
+            if (!ok) break;
+            if (leader) {
                 tc_fence_after();
                 for (int g = 0; g < 2; ++g) {
-                    if (it > 0) {
-                        if (!mbar_wait(p_full + g, (it - 1) & 1, abort)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_pv(g, it - 1);
-                        if (g == 1) tc_commit(kv_empty + ((it - 1) & 1));
-                    }
-                    issue_s(g, it, qb);
-                    tc_commit(s_full + g);
+                    issue_s(g, it, hn & 1);
+                    tc_commit(s_full + g * 2 + (it & 1));
                 }
-                if (ok && t == p.nk - 1) tc_commit(q_empty + qb);
+                if (tn == nk - 1) tc_commit(q_empty + (hn & 1));
             }
-            for (int g = 0; ok && g < 2; ++g) {          // drain: last P V' of both groups
-                if (!mbar_wait(p_full + g, (NT - 1) & 1, abort)) { ok = false; break; }
-                tc_fence_after();
-                issue_pv(g, NT - 1);
-                if (g == 1) tc_commit(kv_empty + ((NT - 1) & 1));
-                tc_commit(s_full + g);
+            __syncwarp();
+            if (++tn == nk) { tn = 0; ++hn; }
+        }
+        for (int it = 0, tp = 0; ok && it < NT; ++it) {
+            const int nx = it + 2;
+            for (int g = 0; g < 2; ++g) {
+                ok = __all_sync(0xffffffffu, mbar_wait(p_full + g * 2 + (it & 1), (it >> 1) & 1, abort));
+                if (!ok) break;
+                if (leader) {
+                    tc_fence_after();
+                    issue_pv(g, it, tp);
+                    tc_commit(o_ready + g * 2 + (it & 1));
+                    if (g == 1) tc_commit(kv_empty + (it & (k2::kStages - 1)));
+                }
+                if (nx < NT) {
+                    if (g == 0) {
+                        ok = s_ready(nx, hn, tn);
+                        if (!ok) break;
+                    }
+                    if (leader) {
+                        tc_fence_after();
+                        issue_s(g, nx, hn & 1);
+                        tc_commit(s_full + g * 2 + (nx & 1));
+                    }
+                }
+                __syncwarp();
             }
-            if (ok && p.last) {                           // output projection: out = u W_o
-                constexpr uint32_t idP = idesc_f16_f32(128, 128);
-                ok = mbar_wait(w_full, 0, abort);
-                const uint32_t wb = smem_u32(sm + k2::kQ);
-                for (int g = 0; ok && g < 2; ++g) {
-                    if (!mbar_wait(u_full + g, 0, abort)) { ok = false; break; }
+            if (ok && nx < NT) {
+                if (leader && tn == nk - 1) tc_commit(q_empty + (hn & 1));
+                if (++tn == nk) { tn = 0; ++hn; }
+            }
+            if (++tp == nk) tp = 0;
+            __syncwarp();
+        }
+        if (ok && p.last) {                           // output projection: out = u W_o
+            constexpr uint32_t idP = idesc_f16_f32(128, 128);
+            ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, abort));
+            for (int g = 0; ok && g < 2; ++g) {
+                ok = __all_sync(0xffffffffu, mbar_wait(u_full + g, 0, abort));
+                if (!ok) break;
+                if (leader) {
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd = sdesc(wb + (kk >> 2) * 16384 + (kk & 3) * 32, 1024, kSwizzle128);
-                        mma_ts(tmem + k2::colS(g), tmem + k2::colU(g) + kk * 8, bd, idP, kk > 0);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
+                               sdesc_at(tV, qbase + (kk >> 2) * 16384 + (kk & 3) * 32), idP, kk > 0 ? 1u : 0u);
                     tc_commit(o_full + g);
                 }
+                __syncwarp();
             }
-            if (!ok) set_abort(abort, p.status, kStatusTimeoutMma);
         }
+        if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutMma);
     } else if (warp < 4) {
-        setmaxnreg_dec<56>();                     // idle warps of the control warpgroup
+        setmaxnreg_dec<88>();                     // idle warps of the control warpgroup
     } else {
-        setmaxnreg_inc<224>();
+        setmaxnreg_inc<208>();
         // ------------------------------------------------------------ softmax warpgroups
         const int g = (warp - 4) >> 2;            // 0: queries xq0..+127, 1: xq0+128..+255
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
         const int x = xq0 + g * 128 + r;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-        const uint32_t tS = tl + k2::colS(g), tO = tl + k2::colO(g), tU = tl + k2::colU(g);
+        const uint32_t tO = tl + k2::colO(g), tU = tl + k2::colU(g);
         const int sboff = g ? k2::kSBb : k2::kSBa;
         float m = -1e30f;                         // running max (log2 units), finite floor
         bool ok = true;
-        for (int it = 0; it <= NT; ++it) {
-            if (!mbar_wait(s_full + g, it & 1, abort)) { ok = false; break; }
-            tc_fence_after();
-            const int h = it / p.nk, t = it % p.nk;
-            if (it > 0 && (t == 0 || it == NT)) {
-                // ---- the previous head is complete: normalise, merge chunks, gate
-                const int hp = h - 1;
-                uint32_t ov[32];
-                tmem_ld32(tO, ov);
-                const float l = __uint_as_float(tmem_ld1(tO + 32));
-                tmem_ld_wait();
-                float o[HD];
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                float lse = l > 0.f ? m + __log2f(l) : -INFINITY;
+
+        // normalise head hp, merge with the running chunk state, gate into u (TMEM)
+        auto finalize = [&](int hp) {
+            uint32_t ov[32];
+            tmem_ld32(tO, ov);
+            const float l = __uint_as_float(tmem_ld1(tO + 32));
+            tmem_ld_wait();
+            float o[HD];
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float lse = l > 0.f ? m + __log2f(l) : -INFINITY;
 #pragma unroll
-                for (int e = 0; e < HD; ++e) o[e] = __uint_as_float(ov[e]) * inv;
-                const size_t srow = ((size_t)(L * NH + hp)) * p.I_pad + x;
-                if (!p.first) {
-                    const float lr = p.lse_run[srow];
-                    const float top = fmaxf(lr, lse);
-                    if (top != -INFINITY) {
-                        const float wr = ex2(lr - top), wc = ex2(lse - top);
-                        const float it_ = 1.f / (wr + wc);
-                        const float4* orun = reinterpret_cast<const float4*>(p.o_run + srow * HD);
+            for (int e = 0; e < HD; ++e) o[e] = __uint_as_float(ov[e]) * inv;
+            const size_t srow = ((size_t)(L * NH + hp)) * p.I_pad + x;
+            if (!p.first) {
+                const float lr = p.lse_run[srow];
+                const float top = fmaxf(lr, lse);
+                if (top != -INFINITY) {
+                    const float wr = ex2(lr - top), wc = ex2(lse - top);
+                    const float it_ = 1.f / (wr + wc);
+                    const float4* orun = reinterpret_cast<const float4*>(p.o_run + srow * HD);
 #pragma unroll
-                        for (int e4 = 0; e4 < HD / 4; ++e4) {
-                            const float4 v = orun[e4];
-                            o[4 * e4 + 0] = (wr * v.x + wc * o[4 * e4 + 0]) * it_;
-                            o[4 * e4 + 1] = (wr * v.y + wc * o[4 * e4 + 1]) * it_;
-                            o[4 * e4 + 2] = (wr * v.z + wc * o[4 * e4 + 2]) * it_;
-                            o[4 * e4 + 3] = (wr * v.w + wc * o[4 * e4 + 3]) * it_;
-                        }
-                        lse = top + __log2f(wr + wc);
+                    for (int e4 = 0; e4 < HD / 4; ++e4) {
+                        const float4 v = orun[e4];
+                        o[4 * e4 + 0] = (wr * v.x + wc * o[4 * e4 + 0]) * it_;
+                        o[4 * e4 + 1] = (wr * v.y + wc * o[4 * e4 + 1]) * it_;
+                        o[4 * e4 + 2] = (wr * v.z + wc * o[4 * e4 + 2]) * it_;
+                        o[4 * e4 + 3] = (wr * v.w + wc * o[4 * e4 + 3]) * it_;
                     }
-                }
-                if (!p.last) {
-                    p.lse_run[srow] = lse;
-                    float4* orun = reinterpret_cast<float4*>(p.o_run + srow * HD);
-#pragma unroll
-                    for (int e4 = 0; e4 < HD / 4; ++e4)
-                        orun[e4] = make_float4(o[4 * e4], o[4 * e4 + 1], o[4 * e4 + 2], o[4 * e4 + 3]);
-                } else {
-                    const uint4* gp = reinterpret_cast<const uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + hp * HD);
-                    uint32_t u[16];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 gv = gp[i];
-                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int e = 8 * i + 2 * jj;
-                            u[4 * i + jj] = pack_f16(f16lo(gw[jj]) * o[e], f16hi(gw[jj]) * o[e + 1]);
-                        }
-                    }
-                    tmem_st16(tU + hp * 16, u);
+                    lse = top + __log2f(wr + wc);
                 }
             }
-            if (it == NT) break;
-
-            // ---- scores of key tile t: S (fp32, TMEM) + bias (f16, smem)
-            const int st = it & 1;
-            if (!mbar_wait(kv_full + st, (it >> 1) & 1, abort)) { ok = false; break; }
-            // two halves of 64 keys: TMEM load (two loads in flight), then the bias add
-            float s[128];
-            const uint8_t* bb = sm + k2::kStage + st * k2::kStageBytes + sboff + r * 128;
+            if (!p.last) {
+                p.lse_run[srow] = lse;
+                float4* orun = reinterpret_cast<float4*>(p.o_run + srow * HD);
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
+                for (int e4 = 0; e4 < HD / 4; ++e4)
+                    orun[e4] = make_float4(o[4 * e4], o[4 * e4 + 1], o[4 * e4 + 2], o[4 * e4 + 3]);
+            } else {
+                const uint4* gp = reinterpret_cast<const uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + hp * HD);
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 gv = gp[i];
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int e = 8 * i + 2 * jj;
+                        u[4 * i + jj] = pack_f16(f16lo(gw[jj]) * o[e], f16hi(gw[jj]) * o[e + 1]);
+                    }
+                }
+                tmem_st16(tU + hp * 16, u);
+            }
+        };
+
+        for (int it = 0, h = 0, t = 0; it < NT; ++it, t = (t + 1 == nk) ? 0 : t + 1, h += (t == 0) ? 1 : 0) {
+            const int b = it & 1, st = it & (k2::kStages - 1);
+            const uint32_t tS = tl + k2::colS(g, b);
+            if (!mbar_wait(s_full + g * 2 + b, (it >> 1) & 1, abort)) { ok = false; break; }
+            if (!mbar_wait(kv_full + st, (it >> 2) & 1, abort)) { ok = false; break; }
+            tc_fence_after();
+            // ---- scores of key tile it: S (fp32, TMEM) + bias (f16, smem)
+            float s[k2::kKT];
+            {
                 uint32_t va[32], vb[32];
-                tmem_ld32(tS + b * 64, va);
-                tmem_ld32(tS + b * 64 + 32, vb);
+                tmem_ld32(tS, va);
+                tmem_ld32(tS + 32, vb);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    s[b * 64 + i] = __uint_as_float(va[i]);
-                    s[b * 64 + 32 + i] = __uint_as_float(vb[i]);
+                    s[i] = __uint_as_float(va[i]);
+                    s[32 + i] = __uint_as_float(vb[i]);
                 }
+            }
+            const uint8_t* bb = sm + k2::kStage + st * k2::kStageBytes + sboff + r * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(bb + b * 16384 + ((c ^ (r & 7)) << 4));
-                    const int k = b * 64 + c * 8;
-                    s[k + 0] = add_f16lo(v.x, s[k + 0]);
-                    s[k + 1] = add_f16hi(v.x, s[k + 1]);
-                    s[k + 2] = add_f16lo(v.y, s[k + 2]);
-                    s[k + 3] = add_f16hi(v.y, s[k + 3]);
-                    s[k + 4] = add_f16lo(v.z, s[k + 4]);
-                    s[k + 5] = add_f16hi(v.z, s[k + 5]);
-                    s[k + 6] = add_f16lo(v.w, s[k + 6]);
-                    s[k + 7] = add_f16hi(v.w, s[k + 7]);
-                }
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(bb + ((c ^ (r & 7)) << 4));
+                const int k = c * 8;
+                s[k + 0] = add_f16lo(v.x, s[k + 0]);
+                s[k + 1] = add_f16hi(v.x, s[k + 1]);
+                s[k + 2] = add_f16lo(v.y, s[k + 2]);
+                s[k + 3] = add_f16hi(v.y, s[k + 3]);
+                s[k + 4] = add_f16lo(v.z, s[k + 4]);
+                s[k + 5] = add_f16hi(v.z, s[k + 5]);
+                s[k + 6] = add_f16lo(v.w, s[k + 6]);
+                s[k + 7] = add_f16hi(v.w, s[k + 7]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(kv_empty + st);
-            const int k0 = p.k_begin + t * 128;
-            if (k0 + 128 > p.k_end) {                    // ragged last tile of the key range
+            const int k0 = p.k_begin + t * k2::kKT;
+            if (k0 + k2::kKT > p.k_end) {                // ragged last tile of the key range
                 const int nvalid = p.k_end - k0;
 #pragma unroll
-                for (int k = 0; k < 128; ++k)
+                for (int k = 0; k < k2::kKT; ++k)
                     if (k >= nvalid) s[k] = -INFINITY;
             }
             // tile max: four independent 3-input max chains
             float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
 #pragma unroll
-            for (int k = 4; k < 128; k += 8) {
+            for (int k = 4; k < k2::kKT; k += 8) {
                 m0 = max3(m0, s[k], s[k + 1]);
                 m1 = max3(m1, s[k + 2], s[k + 3]);
                 m2 = max3(m2, s[k + 4], s[k + 5]);
                 m3 = max3(m3, s[k + 6], s[k + 7]);
             }
             const float mt = fmaxf(max3(m0, m1, m2), m3);
+            // P V'(it-2) is long complete: waiting for it keeps the o_ready phases in
+            // step at no cost.  P V'(it-1) is waited for only when O is about to be
+            // read: at a head boundary (finalize) or for a rescale, which is rare.
+            // A second wait on that already completed phase (at tile it+1) returns at
+            // once, because P V'(it+1) cannot complete before P(it+1) is written.
+            if (it >= 2 && !mbar_wait(o_ready + g * 2 + (it & 1), ((it - 2) >> 1) & 1, abort)) { ok = false; break; }
+            auto wait_prev_pv = [&]() -> bool {
+                if (!mbar_wait(o_ready + g * 2 + ((it - 1) & 1), ((it - 1) >> 1) & 1, abort)) return false;
+                tc_fence_after();
+                return true;
+            };
             if (t == 0) {
+                if (it > 0) {
+                    if (!wait_prev_pv()) { ok = false; break; }
+                    finalize(h - 1);
+                }
                 m = fmaxf(mt, -1e30f);
             } else {
                 const bool need = mt > m + 8.f;          // rescale only when the max grew by > 2^8
                 if (__any_sync(0xffffffffu, need)) {
+                    if (!wait_prev_pv()) { ok = false; break; }
                     uint32_t ov[32];
                     tmem_ld32(tO, ov);
                     uint32_t lv = tmem_ld1(tO + 32);
@@ -758,16 +827,20 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 }
             }
             const float negm = -m;
-            uint32_t pk[64];
+            uint32_t pk[32];
 #pragma unroll
-            for (int k = 0; k < 128; k += 2)
-                pk[k >> 1] = k2::kExpF16x2 ? exp2_pair_f16x2(s[k], s[k + 1], negm) : exp2_pair_f32(s[k], s[k + 1], negm);
+            for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
             tmem_st32(tS, pk);
-            tmem_st32(tS + 32, pk + 32);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + g);
+            if (lane == 0) mbar_arrive(p_full + g * 2 + b);
+        }
+        if (ok && NT >= 2) ok = mbar_wait(o_ready + g * 2 + (NT & 1), ((NT - 2) >> 1) & 1, abort);
+        if (ok) ok = mbar_wait(o_ready + g * 2 + ((NT - 1) & 1), ((NT - 1) >> 1) & 1, abort);
+        if (ok) {
+            tc_fence_after();
+            finalize(NH - 1);
         }
         if (!ok) set_abort(abort, p.status, kStatusTimeoutSoftmax);
         if (ok && p.last) {
@@ -780,10 +853,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
                 const size_t pair = p.node == TRI_ATTN_STARTING ? (size_t)L * p.I + x : (size_t)x * p.I + L;
                 uint4* dst = reinterpret_cast<uint4*>(p.out + pair * CZ);
+                const uint32_t tOut = tl + k2::colS(g, 0);
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t v[32];
-                    tmem_ld32(tS + cb * 32, v);
+                    tmem_ld32(tOut + cb * 32, v);
                     tmem_ld_wait();
                     uint32_t o[16];
 #pragma unroll
@@ -962,7 +1036,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     CUtensorMap mQ, mK, mV, mB, mWo;
     const uint64_t rows_qk = (uint64_t)I * NH * Ip;
     if (!map2d(&mQ, hf(W.q), HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !map2d(&mK, hf(W.k), HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mK, hf(W.k), HD, rows_qk, HD * 2, HD, k2::kKT, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !map2d(&mV, hf(W.v), Ip, (uint64_t)I * NH * HD, (uint64_t)Ip * 2, 64, HD, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !map2d(&mB, hf(W.bias), Ip, (uint64_t)NH * Ip, (uint64_t)Ip * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !map2d(&mWo, hf(W.wo_t), CH, CZ, CH * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -976,7 +1050,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.I_pad = Ip;
         ap.k_begin = k0;
         ap.k_end = k1e;
-        ap.nk = (k1e - k0 + 127) / 128;
+        ap.nk = (k1e - k0 + k2::kKT - 1) / k2::kKT;
         ap.first = k0 == 0;
         ap.last = k1e == I;
         ap.mask = a.mask;

@@ -62,6 +62,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// One lane of the (converged) warp is elected; all lanes get the same answer
+// pattern (true on exactly one lane).  Keeping the control warps' loops
+// converged lets warp-uniform values (descriptors, addresses) stay uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, %1;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -137,6 +149,14 @@ constexpr uint32_t kSwizzle64 = 4;
 // Shared-memory matrix descriptor for a K-major, swizzled operand: rows of
 // (swizzle width) bytes, 8-row groups `sbo` bytes apart.  Advancing K inside
 // the swizzle atom is done by adding the byte offset to the start address.
+__host__ __device__ __forceinline__ constexpr uint64_t sdesc_tmpl(uint32_t sbo, uint32_t swizzle) {
+    return (static_cast<uint64_t>(1u) << 16) | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (static_cast<uint64_t>(1u) << 46) | (static_cast<uint64_t>(swizzle) << 61);
+}
+// descriptor template + start address (16-byte units)
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t tmpl, uint32_t saddr) {
+    return tmpl | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+}
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo, uint32_t swizzle) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
