@@ -166,7 +166,7 @@ int tri_attn_kernel_times(tri_attn_ctx* ctx, const char** names, float* ms, int 
  * device memory is fully reserved up front.  They can use neither the
  * caller-allocated workspace of tri_attn_forward nor tri_attn_create (which
  * allocates the status word).  This entry point needs neither: its workspace
- * is a file-scope device array of the library (33.5 MB: the sm103 workspace
+ * is a file-scope device array of the library (34.3 MB: the sm103 workspace
  * at I = 128 plus a status word), which every GPU that loads the library
  * holds until the process exits.  The paper has no counterpart of it.
  *

@@ -62,7 +62,12 @@ constexpr int NPROJ = 4 * CH;      // 512 MMA output columns in four groups of 1
 constexpr int kGroupQ = 0, kGroupV = 1, kGroupK = 2, kGroupG = 3;
 constexpr int NCONST = NPROJ + NH; // + pair bias columns
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kQPad = 256;         // token padding of the sm103 workspace (query-tile pair)
+// Pair bias of a masked or padded key, log2 units.  Finite (not -inf) because the
+// bias enters S through an MMA with an identity matrix, where 0 x -inf would be
+// NaN; 2^-30000 is exactly 0 in fp32, so such keys still get probability 0 (and
+// if every key so far was masked, the first real key's rescale factor 2^-30000
+// removes their contribution exactly).
+constexpr float kMaskedBias = -30000.f;
 
 // Block-uniform read of the device status word (one thread reads, all see the
 // same value), so an early return never splits a block at a later barrier.
@@ -82,7 +87,7 @@ __device__ __forceinline__ void set_abort(volatile int* abort, uint32_t* status,
 // Weight preparation
 // =====================================================================================
 struct PrepArgs {
-    const float *gamma, *beta, *b_o;
+    const float *gamma, *beta, *b_o, *b_g;
     const __nv_bfloat16 *w_q, *w_k, *w_v, *w_g, *w_b, *w_o;
     __nv_bfloat16* wprep;   // [512][128]  row n = (gamma . W)[:, n], K-major for the MMA
     float* colsum;          // [516]       sum_c of the (rounded) gamma.W column
@@ -90,6 +95,8 @@ struct PrepArgs {
     float* wb32;            // [128][4]    gamma . W_b in fp32
     __half* wo_t;           // [128][128]  W_o transposed (f16): row n = W_o[:, n]
     float* bo;              // [128]
+    float* cst;             // [256][4]    per column pair {colsum(n), colsum(n+1), off(n), off(n+1)},
+                            //             off = scale * beta W (+ b_g for the gate group)
 };
 
 __global__ void __launch_bounds__(128) sm103_prep(PrepArgs a) {
@@ -122,8 +129,17 @@ __global__ void __launch_bounds__(128) sm103_prep(PrepArgs a) {
         }
         __syncthreads();
         if (c == 0) {
-            a.colsum[n] = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-            a.betaw[n] = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+            const float cs = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+            const float bw = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+            a.colsum[n] = cs;
+            a.betaw[n] = bw;
+            if (n < NPROJ) {
+                const int which = n / CH;
+                const float sc = which == kGroupQ ? kLog2e * rsqrtf((float)HD) : 1.f;
+                const float off = bw * sc + (which == kGroupG ? a.b_g[n % CH] : 0.f);
+                a.cst[(n >> 1) * 4 + (n & 1)] = cs;
+                a.cst[(n >> 1) * 4 + 2 + (n & 1)] = off;
+            }
         }
     } else {
         const int row = n - NCONST;           // output channel of W_o
@@ -139,7 +155,7 @@ struct ProjParams {
     int node, I, I_pad, ntx, ntiles;
     float eps;
     const uint8_t* mask;
-    const float *colsum, *betaw, *wb32, *b_g;
+    const float *colsum, *betaw, *wb32, *cst;
     __half *q, *k, *vt, *g, *bias;     // f16 intermediates
     uint32_t* status;
 };
@@ -148,8 +164,8 @@ namespace k1 {
 constexpr int kThreads = 320;                // 2 epilogue warpgroups + producer warp + MMA warp
 constexpr int kW = 0;                        // 4 x 32 KB: [half(qk|vg)][k-half][256 rows][128 B]
 constexpr int kZ = 131072;                   // 2 stages x 32 KB: [k-half][128 rows][128 B]
-constexpr int kConst = kZ + 2 * 32768;       // colsum[516] betaw[516] wb32[512] b_g[128]
-constexpr int kConstBytes = (NCONST * 2 + CZ * NH + CH) * 4;
+constexpr int kConst = kZ + 2 * 32768;       // cst[256][4], wb32[128][4], bias colsum[4], bias offset[4]
+constexpr int kConstBytes = (256 * 4 + CZ * NH + 2 * NH) * 4;
 constexpr int kBar = kConst + ((kConstBytes + 127) / 128) * 128;
 constexpr int kSmem = kBar + 256 + 1024;     // + alignment slack
 }  // namespace k1
@@ -160,10 +176,10 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* s_colsum = reinterpret_cast<float*>(sm + k1::kConst);
-    float* s_betaw = s_colsum + NCONST;
-    float* s_wb = s_betaw + NCONST;        // [128][4]
-    float* s_bg = s_wb + CZ * NH;          // [128]
+    float* s_cst = reinterpret_cast<float*>(sm + k1::kConst);   // [256][4]
+    float* s_wb = s_cst + 256 * 4;         // [128][4]
+    float* s_bcs = s_wb + CZ * NH;         // [4] pair-bias column sums
+    float* s_bbw = s_bcs + NH;             // [4] pair-bias beta W
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k1::kBar);
     uint64_t* w_full = bars + 0;
     uint64_t* z_full = bars + 1;      // [2]
@@ -174,12 +190,12 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 11);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < NCONST; i += blockDim.x) {
-        s_colsum[i] = p.colsum[i];
-        s_betaw[i] = p.betaw[i];
-    }
+    for (int i = threadIdx.x; i < 256 * 4; i += blockDim.x) s_cst[i] = p.cst[i];
     for (int i = threadIdx.x; i < CZ * NH; i += blockDim.x) s_wb[i] = p.wb32[i];
-    for (int i = threadIdx.x; i < CH; i += blockDim.x) s_bg[i] = p.b_g[i];
+    if (threadIdx.x < NH) {
+        s_bcs[threadIdx.x] = p.colsum[NPROJ + threadIdx.x];
+        s_bbw[threadIdx.x] = p.betaw[NPROJ + threadIdx.x];
+    }
     if (threadIdx.x == 0) {
         mbar_init(w_full, 1);
         for (int s = 0; s < 2; ++s) {
@@ -314,8 +330,8 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 const float bh[NH] = {bh0, bh1, bh2, bh3};
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
-                    const float v = (fmaf(bh[h], rstd, nmr * s_colsum[NPROJ + h]) + s_betaw[NPROJ + h]) * kLog2e;
-                    p.bias[((size_t)h * p.I_pad + L) * p.I_pad + x] = __float2half_rn(valid ? v : -INFINITY);
+                    const float v = (fmaf(bh[h], rstd, nmr * s_bcs[h]) + s_bbw[h]) * kLog2e;
+                    p.bias[((size_t)h * p.I_pad + L) * p.I_pad + x] = __float2half_rn(valid ? v : kMaskedBias);
                 }
             }
 
@@ -324,51 +340,46 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 break;
             }
             tc_fence_after();
-            // 32 accumulator columns -> normalised, transformed f16 values -> global
+            // 32 accumulator columns -> normalised, transformed f16 values -> global.
+            // value = r * (acc - mu * colsum) + off, two columns per packed FMA, with
+            // r = rstd (times log2(e)/sqrt(d) for q) and off from the prepared constants.
+            const float rq = rstd * (kLog2e * rsqrtf((float)HD));
+            const float nmu = -mu;
             auto emit = [&](int cb, const uint32_t (&acc)[32]) {
                 const int n0 = wg * 256 + cb * 32;
                 const int which = n0 / CH, h = (n0 % CH) / HD;
+                const float rr = which == kGroupQ ? rq : rstd;
+                const float4* cst = reinterpret_cast<const float4*>(s_cst) + (n0 >> 1);
                 uint32_t o[16];
-                if (which == kGroupG) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float v0 = fmaf(__uint_as_float(acc[e]), rstd, nmr * s_colsum[n0 + e]) + s_betaw[n0 + e];
-                        float v1 = fmaf(__uint_as_float(acc[e + 1]), rstd, nmr * s_colsum[n0 + e + 1]) +
-                                   s_betaw[n0 + e + 1];
-                        v0 += s_bg[h * HD + e];
-                        v1 += s_bg[h * HD + e + 1];
-                        v0 = 1.f / (1.f + ex2(-v0 * kLog2e));
-                        v1 = 1.f / (1.f + ex2(-v1 * kLog2e));
-                        o[e >> 1] = pack_f16(v0, v1);
+                for (int e = 0; e < 32; e += 2) {
+                    const float4 c = cst[e >> 1];
+                    float t0, t1, v0, v1;
+                    fma2(t0, t1, nmu, nmu, c.x, c.y, __uint_as_float(acc[e]), __uint_as_float(acc[e + 1]));
+                    fma2(v0, v1, rr, rr, t0, t1, c.z, c.w);
+                    if (which == kGroupG) {               // sigmoid(v) = 0.5 tanh(v / 2) + 0.5
+                        v0 = fmaf(0.5f, tanh_approx(0.5f * v0), 0.5f);
+                        v1 = fmaf(0.5f, tanh_approx(0.5f * v1), 0.5f);
                     }
+                    o[e >> 1] = pack_f16(v0, v1);
+                }
+                const size_t lh = (size_t)L * NH + h;
+                if (which == kGroupG) {
                     uint4* dst = reinterpret_cast<uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + h * HD);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                } else {
-                    const float sc = which == kGroupQ ? qscale : 1.f;
-                    const float r2 = rstd * sc, n2 = nmr * sc;
+                } else if (which == kGroupV) {
+                    unsigned short* dst = reinterpret_cast<unsigned short*>(p.vt + lh * HD * p.I_pad + x);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float v0 = fmaf(__uint_as_float(acc[e]), r2, fmaf(n2, s_colsum[n0 + e], s_betaw[n0 + e] * sc));
-                        const float v1 = fmaf(__uint_as_float(acc[e + 1]), r2,
-                                              fmaf(n2, s_colsum[n0 + e + 1], s_betaw[n0 + e + 1] * sc));
-                        o[e >> 1] = pack_f16(v0, v1);
+                        dst[(size_t)e * p.I_pad] = static_cast<unsigned short>(o[e >> 1] & 0xFFFFu);
+                        dst[(size_t)(e + 1) * p.I_pad] = static_cast<unsigned short>(o[e >> 1] >> 16);
                     }
-                    const size_t lh = (size_t)L * NH + h;
-                    if (which == kGroupV) {
-                        unsigned short* dst = reinterpret_cast<unsigned short*>(p.vt + lh * HD * p.I_pad + x);
+                } else {
+                    __half* base = which == kGroupQ ? p.q : p.k;
+                    uint4* dst = reinterpret_cast<uint4*>(base + (lh * p.I_pad + x) * HD);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            dst[(size_t)e * p.I_pad] = static_cast<unsigned short>(o[e >> 1] & 0xFFFFu);
-                            dst[(size_t)(e + 1) * p.I_pad] = static_cast<unsigned short>(o[e >> 1] >> 16);
-                        }
-                    } else {
-                        __half* base = which == kGroupQ ? p.q : p.k;
-                        uint4* dst = reinterpret_cast<uint4*>(base + (lh * p.I_pad + x) * HD);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                    }
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                 }
             };
 #pragma unroll 1
@@ -417,7 +428,8 @@ constexpr int kSV = 4096;                    // V' tile: 32 rows V^T + 16 rows [
 constexpr int kSBa = 10240, kSBb = 26624;    // bias tiles of the two query tiles: 128 rows x 128 B (SW128)
 constexpr int kStageBytes = 43008;
 constexpr int kStageTx = 4096 + 4096 + 32768;   // bytes the TMA writes per stage
-constexpr int kBar = kStage + kStages * kStageBytes;
+constexpr int kIdent = kStage + kStages * kStageBytes;   // 64 x 64 f16 identity (SW128, K-major)
+constexpr int kBar = kIdent + 8192;
 constexpr int kSmem = kBar + 512 + 1024;     // barriers + alignment slack
 // TMEM columns
 __host__ __device__ constexpr uint32_t colS(int g, int b) { return g * 128u + b * 64u; }   // S / P buffers
@@ -476,6 +488,18 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const uint32_t one2 = off < 128 ? 0x3C003C00u : 0u;
         *reinterpret_cast<uint4*>(dst) = make_uint4(one2, one2, one2, one2);
     }
+    // 64 x 64 identity, the B operand that adds the staged bias tile into S:
+    // S = Q K^T + Bias I (row n holds 1.0 at column n; 128B-swizzled rows).
+    for (int i = threadIdx.x; i < 8192 / 16; i += blockDim.x) {
+        const int n = i >> 3, c = i & 7;                      // row n, physical 16-byte chunk c
+        const int lc = c ^ (n & 7);                           // logical chunk: columns 8 lc .. 8 lc + 7
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if ((n >> 3) == lc) {
+            const int e = n & 7;                              // column n within the chunk
+            w[e >> 1] = (e & 1) ? 0x3C000000u : 0x00003C00u;
+        }
+        *reinterpret_cast<uint4*>(sm + k2::kIdent + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
     fence_proxy_async_smem();
 
     const int nk = p.nk;
@@ -489,7 +513,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
         for (int s = 0; s < k2::kStages; ++s) {
             mbar_init(kv_full + s, 1);
-            mbar_init(kv_empty + s, 1 + 8);
+            mbar_init(kv_empty + s, 1);
             mbar_init(s_full + s, 1);
             mbar_init(p_full + s, 4);
             mbar_init(o_ready + s, 1);
@@ -508,15 +532,15 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const uint32_t tmem = *tmem_holder;
 
     // Register budget: launched at 168 per thread.  The control warpgroup
-    // (warps 0-3, one warp per SM sub-partition) drops to 88 and each softmax
-    // warp grows to 208, so every sub-partition releases exactly what it takes
-    // (32 x 80 = 2 x 32 x 40 registers) and no increase can wait on another
+    // (warps 0-3, one warp per SM sub-partition) drops to 120 and each softmax
+    // warp grows to 192, so every sub-partition releases exactly what it takes
+    // (32 x 48 = 2 x 32 x 24 registers) and no increase can wait on another
     // sub-partition.
     // The producer and MMA warps run their loops converged (every lane waits on the
     // same barriers, so loop control and addresses stay warp-uniform) and one
     // elected lane issues each TMA copy or tcgen05 instruction.
     if (warp == 0) {
-        setmaxnreg_dec<88>();
+        setmaxnreg_dec<120>();
         // ------------------------------------------------------------ TMA producer
         const bool leader = elect_one();
         if (leader) {
@@ -569,7 +593,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
     } else if (warp == 1) {
-        setmaxnreg_dec<88>();
+        setmaxnreg_dec<120>();
         // ------------------------------------------------------------ MMA issuer
         const bool leader = elect_one();
         constexpr uint32_t idS = idesc_f16_f32(128, k2::kKT);
@@ -584,12 +608,21 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         constexpr uint64_t kStageStep = k2::kStageBytes >> 4;
         bool ok = true;
         // S_g(it) = Q_g K(it)^T into buffer it & 1 (head parity qb)
+        // S_g(it) = Q_g K(it)^T + Bias_g(it) I into buffer it & 1: the pair bias is
+        // added by the tensor core (the staged bias tile is the A operand of four
+        // more K-steps against a 64 x 64 identity).
+        const uint64_t dB0 = sdesc_at(tV, sbase + k2::kSBa), dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
+        constexpr uint64_t kBiasStep = (k2::kSBb - k2::kSBa) >> 4;
         auto issue_s = [&](int g, int it, int qb) {
             const uint64_t qa = dQ0 + static_cast<uint64_t>(qb * 1024 + g * 512);
-            const uint64_t kb = dK0 + static_cast<uint64_t>(it & (k2::kStages - 1)) * kStageStep;
+            const uint64_t st = static_cast<uint64_t>(it & (k2::kStages - 1));
+            const uint64_t kb = dK0 + st * kStageStep;
+            const uint64_t bb = dB0 + st * kStageStep + static_cast<uint64_t>(g) * kBiasStep;
             const uint32_t d = tmem + k2::colS(g, it & 1);
             mma_ss(d, qa, kb, idS, 0u);
             mma_ss(d, qa + 2, kb + 2, idS, 1u);
+#pragma unroll
+            for (int kk = 0; kk < k2::kKT / 16; ++kk) mma_ss(d, bb + kk * 2, dI + kk * 2, idS, 1u);
         };
         // O_g (+)= P_g(it) V'(it); the first tile of a head (t == 0) overwrites
         auto issue_pv = [&](int g, int it, int t) {
@@ -672,9 +705,9 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutMma);
     } else if (warp < 4) {
-        setmaxnreg_dec<88>();                     // idle warps of the control warpgroup
+        setmaxnreg_dec<120>();                     // idle warps of the control warpgroup
     } else {
-        setmaxnreg_inc<208>();
+        setmaxnreg_inc<192>();
         // ------------------------------------------------------------ softmax warpgroups
         const int g = (warp - 4) >> 2;            // 0: queries xq0..+127, 1: xq0+128..+255
         const int wq = warp & 3;
@@ -682,7 +715,6 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int x = xq0 + g * 128 + r;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tO = tl + k2::colO(g), tU = tl + k2::colU(g);
-        const int sboff = g ? k2::kSBb : k2::kSBa;
         float m = -1e30f;                         // running max (log2 units), finite floor
         bool ok = true;
 
@@ -740,12 +772,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         };
 
         for (int it = 0, h = 0, t = 0; it < NT; ++it, t = (t + 1 == nk) ? 0 : t + 1, h += (t == 0) ? 1 : 0) {
-            const int b = it & 1, st = it & (k2::kStages - 1);
+            const int b = it & 1;
             const uint32_t tS = tl + k2::colS(g, b);
             if (!mbar_wait(s_full + g * 2 + b, (it >> 1) & 1, abort)) { ok = false; break; }
-            if (!mbar_wait(kv_full + st, (it >> 2) & 1, abort)) { ok = false; break; }
             tc_fence_after();
-            // ---- scores of key tile it: S (fp32, TMEM) + bias (f16, smem)
+            // ---- scores of key tile it (bias already added by the tensor core)
             float s[k2::kKT];
             {
                 uint32_t va[32], vb[32];
@@ -758,22 +789,6 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     s[32 + i] = __uint_as_float(vb[i]);
                 }
             }
-            const uint8_t* bb = sm + k2::kStage + st * k2::kStageBytes + sboff + r * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = *reinterpret_cast<const uint4*>(bb + ((c ^ (r & 7)) << 4));
-                const int k = c * 8;
-                s[k + 0] = add_f16lo(v.x, s[k + 0]);
-                s[k + 1] = add_f16hi(v.x, s[k + 1]);
-                s[k + 2] = add_f16lo(v.y, s[k + 2]);
-                s[k + 3] = add_f16hi(v.y, s[k + 3]);
-                s[k + 4] = add_f16lo(v.z, s[k + 4]);
-                s[k + 5] = add_f16hi(v.z, s[k + 5]);
-                s[k + 6] = add_f16lo(v.w, s[k + 6]);
-                s[k + 7] = add_f16hi(v.w, s[k + 7]);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(kv_empty + st);
             const int k0 = p.k_begin + t * k2::kKT;
             if (k0 + k2::kKT > p.k_end) {                // ragged last tile of the key range
                 const int nvalid = p.k_end - k0;
@@ -944,32 +959,6 @@ bool sm103_supported(int c_z, int H, int d, int dtype) {
     return dtype == TRI_ATTN_BF16 && c_z == CZ && H == NH && d == HD;
 }
 
-Workspace sm103_layout(int I, int key_chunks) {
-    Workspace w;
-    w.I = I;
-    w.I_pad = round_up(I, kQPad);
-    const size_t P = (size_t)I * w.I_pad;
-    size_t off = 0;
-    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
-    w.wprep = take((size_t)NPROJ * CZ * 2);
-    w.colsum = take(NCONST * 4);
-    w.betaw = take(NCONST * 4);
-    w.wb32 = take(CZ * NH * 4);
-    w.wo_t = take((size_t)CZ * CH * 2);
-    w.bo = take(CZ * 4);
-    w.q = take(P * CH * 2);
-    w.k = take(P * CH * 2);
-    w.v = take(P * CH * 2);
-    w.g = take(P * CH * 2);
-    w.bias = take((size_t)NH * w.I_pad * w.I_pad * 2);
-    if (key_chunks > 1) {
-        w.o_run = take(P * CH * 4);
-        w.lse_run = take(P * NH * 4);
-    }
-    w.total = off;
-    return w;
-}
-
 cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     const Workspace& W = *a.lay;
     char* ws = a.ws;
@@ -988,11 +977,11 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     }
 
     // ---- weight preparation
-    PrepArgs pa{a.w.ln_gamma, a.w.ln_beta, a.w.b_o,
+    PrepArgs pa{a.w.ln_gamma, a.w.ln_beta, a.w.b_o, a.w.b_g,
                 static_cast<const __nv_bfloat16*>(a.w.w_q), static_cast<const __nv_bfloat16*>(a.w.w_k),
                 static_cast<const __nv_bfloat16*>(a.w.w_v), static_cast<const __nv_bfloat16*>(a.w.w_g),
                 static_cast<const __nv_bfloat16*>(a.w.w_b), static_cast<const __nv_bfloat16*>(a.w.w_o),
-                bf(W.wprep), f32(W.colsum), f32(W.betaw), f32(W.wb32), hf(W.wo_t), f32(W.bo)};
+                bf(W.wprep), f32(W.colsum), f32(W.betaw), f32(W.wb32), hf(W.wo_t), f32(W.bo), f32(W.cst)};
     if (tm) tm->begin("sm103_prep", s);
     sm103_prep<<<NCONST + CZ, 128, 0, s>>>(pa);
     if (tm) tm->end(s);
@@ -1016,7 +1005,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     pp.colsum = f32(W.colsum);
     pp.betaw = f32(W.betaw);
     pp.wb32 = f32(W.wb32);
-    pp.b_g = a.w.b_g;
+    pp.cst = f32(W.cst);
     pp.q = hf(W.q);
     pp.k = hf(W.k);
     pp.vt = hf(W.v);

@@ -20,8 +20,8 @@ namespace tri_attn {
 
 constexpr int kTile = 128;          // token padding granule (one MMA tile of keys or queries)
 
-inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
-inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
+constexpr size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
 // Device status word bits (set by bounded waits that gave up).
 enum : uint32_t {
@@ -39,6 +39,7 @@ struct Workspace {
     size_t q = 0, k = 0, v = 0, g = 0, bias = 0, u = 0;   // projections
     size_t o_run = 0, lse_run = 0;                          // key-chunk state (0 bytes if unchunked)
     size_t wprep = 0, colsum = 0, betaw = 0, wb32 = 0, wo_t = 0, bo = 0;  // prepared weights (sm103)
+    size_t cst = 0;                                          // per column pair {colsum x2, offset x2} (sm103)
     size_t total = 0;
 };
 
@@ -71,7 +72,35 @@ cudaError_t simt_forward(const FwdArgs& a, int dtype, cudaStream_t s, LaunchTime
 
 // sm103 path (bf16, c_z = 128, H = 4, d = 32).
 bool sm103_supported(int c_z, int H, int d, int dtype);
-Workspace sm103_layout(int I, int key_chunks);
+
+// Workspace of the sm103 path (usable at compile time: the allocation-free entry
+// point sizes its device array with it).  Tokens are padded to a multiple of 256.
+constexpr Workspace sm103_layout(int I, int key_chunks) {
+    Workspace w;
+    w.I = I;
+    w.I_pad = round_up(I, 256);
+    const size_t P = (size_t)I * w.I_pad;
+    size_t off = 0;
+    auto take = [&off](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    w.wprep = take((size_t)512 * 128 * 2);   // (gamma . W)^T for q | v | k | g, bf16
+    w.colsum = take(516 * 4);
+    w.betaw = take(516 * 4);
+    w.wb32 = take(128 * 4 * 4);
+    w.wo_t = take((size_t)128 * 128 * 2);    // W_o^T, f16
+    w.bo = take(128 * 4);
+    w.cst = take(256 * 4 * 4);
+    w.q = take(P * 128 * 2);
+    w.k = take(P * 128 * 2);
+    w.v = take(P * 128 * 2);
+    w.g = take(P * 128 * 2);
+    w.bias = take((size_t)4 * w.I_pad * w.I_pad * 2);
+    if (key_chunks > 1) {
+        w.o_run = take(P * 128 * 4);
+        w.lse_run = take(P * 4 * 4);
+    }
+    w.total = off;
+    return w;
+}
 cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* t);
 
 // Chunk bounds shared by both paths: size = round_up(ceil(I / n), 8).

@@ -9,7 +9,7 @@
 // tri_attn_create allocates.
 //
 // The scratch array below is part of the module: every GPU on which the
-// library's module is loaded holds it (kStaticScratchBytes, about 33 MB)
+// library's module is loaded holds it (kStaticScratchBytes, 34.3 MB)
 // until the process exits.  Host code cannot use the array's name as a device
 // address (it names a host-side stand-in), so the device address is obtained
 // once per device with cudaGetSymbolAddress, with that device current, and
@@ -22,7 +22,7 @@ namespace tri_attn {
 namespace {
 
 constexpr int kStaticImax = 128;                      // largest I this entry point accepts
-constexpr size_t kStaticWorkspace = 34249728;         // sm103 workspace bytes at I = 128, unchunked
+constexpr size_t kStaticWorkspace = sm103_layout(kStaticImax, 1).total;   // sm103 workspace at I = 128
 constexpr size_t kStaticScratchBytes = kStaticWorkspace + 256;   // + the device status word
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
