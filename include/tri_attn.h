@@ -187,6 +187,17 @@ int tri_attn_kernel_times(tri_attn_ctx* ctx, const char** names, float* ms, int 
 tri_attn_status tri_attn_forward_static(int node, int I, const void* Z, const uint8_t* token_mask,
                                         const tri_attn_weights* w, float ln_eps, void* out, void* stream);
 
+/* Test hook for the failure path (no GPU fault is involved).
+ * fault = TRI_ATTN_FAULT_SKIP_STAGE: the next tri_attn_forward of this context
+ * runs its attention kernel with the first block's producer skipping one K/V
+ * stage load, so that block's bounded waits run out (about 2 s), it records the
+ * timeout in the status word and exits, and later blocks of the launch exit at
+ * once; tri_attn_status_sync then returns TRI_ATTN_ETIMEOUT and clears the
+ * word, after which the context is fully usable.  The hook applies to one
+ * forward; fault = 0 clears it.  EUNSUPPORTED on the SIMT path. */
+enum { TRI_ATTN_FAULT_NONE = 0, TRI_ATTN_FAULT_SKIP_STAGE = 1 };
+tri_attn_status tri_attn_debug_inject(tri_attn_ctx* ctx, int fault);
+
 /* Static description of a status code. */
 const char* tri_attn_status_string(int status);
 

@@ -21,7 +21,8 @@ NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
 
 EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
            "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
-           "tri_attn_status_string", "tri_attn_forward_static")
+           "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject")
+FAULT_NONE, FAULT_SKIP_STAGE = 0, 1
 
 
 class TriAttnError(RuntimeError):
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tri_attn_kernel_times.restype = i
     lib.tri_attn_forward_static.argtypes = [i, i, vp, vp, ctypes.POINTER(Weights), ctypes.c_float, vp, vp]
     lib.tri_attn_forward_static.restype = i
+    lib.tri_attn_debug_inject.argtypes = [vp, i]
+    lib.tri_attn_debug_inject.restype = i
     lib.tri_attn_status_string.argtypes = [i]
     lib.tri_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -174,6 +177,10 @@ class TriAttn:
 
     def status_sync(self, stream=None) -> int:
         return self.lib.tri_attn_status_sync(self._h, _stream_ptr(stream))
+
+    def debug_inject(self, fault: int) -> int:
+        """Test hook: the next forward's attention kernel has one block whose bounded waits run out."""
+        return self.lib.tri_attn_debug_inject(self._h, fault)
 
     def set_timing(self, on: bool) -> None:
         self.lib.tri_attn_set_timing(self._h, int(on))

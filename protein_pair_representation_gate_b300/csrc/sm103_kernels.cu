@@ -409,6 +409,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
 // =====================================================================================
 struct AttnParams {
     int node, I, I_pad, nk, k_begin, k_end, first, last;
+    int inject;                // test hook: block (0,0) skips the load of stage 1
     const uint8_t* mask;
     const __half* g;
     const float* bo;
@@ -418,7 +419,7 @@ struct AttnParams {
 };
 
 namespace k2 {
-constexpr int kThreads = 384;                // control warpgroup (producer, MMA, 2 idle) + 2 softmax warpgroups
+constexpr int kThreads = 384;                // control warpgroup (producer, 2 MMA issuers, 1 idle) + 2 softmax warpgroups
 constexpr int kKT = 64;                      // keys per stage (one S sub-tile)
 constexpr int kStages = 4;                  // power of two: stage = it & 3, phase = (it >> 2) & 1
 constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64); W_o at the end
@@ -507,13 +508,13 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(q_full + s, 1);
-            mbar_init(q_empty + s, 1);
+            mbar_init(q_empty + s, 2);            // one commit per MMA issuer
             mbar_init(u_full + s, 4);
             mbar_init(o_full + s, 1);
         }
         for (int s = 0; s < k2::kStages; ++s) {
             mbar_init(kv_full + s, 1);
-            mbar_init(kv_empty + s, 1);
+            mbar_init(kv_empty + s, 2);           // one commit per MMA issuer (softmax group)
             mbar_init(s_full + s, 1);
             mbar_init(p_full + s, 4);
             mbar_init(o_ready + s, 1);
@@ -566,7 +567,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 }
                 ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it >> 2) & 1) ^ 1, abort));
                 if (!ok) break;
-                if (leader) {
+                const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && blockIdx.x == 0 && blockIdx.y == 0;
+                if (leader && !skip) {
                     const int k0 = p.k_begin + t * k2::kKT;
                     uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
                     mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
@@ -592,32 +594,33 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2) {
         setmaxnreg_dec<120>();
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues every MMA of softmax group 0, warp 2 those of group 1, so
+        // each group's P -> P V' -> S(it+2) round trip waits only on its own group.
+        const int g = warp - 1;
         const bool leader = elect_one();
         constexpr uint32_t idS = idesc_f16_f32(128, k2::kKT);
         constexpr uint32_t idO = idesc_f16_f32(128, 48);
         constexpr uint64_t tK = sdesc_tmpl(512, kSwizzle64);      // Q and K tiles: 64 B rows
-        constexpr uint64_t tV = sdesc_tmpl(1024, kSwizzle128);    // V' and W_o^T: 128 B rows
+        constexpr uint64_t tV = sdesc_tmpl(1024, kSwizzle128);    // V', bias, W_o^T: 128 B rows
         const uint32_t qbase = smem_u32(sm + k2::kQ), sbase = smem_u32(sm + k2::kStage);
-        // descriptors of stage 0 / Q buffer 0; other stages and buffers are fixed
-        // offsets in the 16-byte address field (no carry: shared addresses < 256 KB)
-        const uint64_t dQ0 = sdesc_at(tK, qbase), dK0 = sdesc_at(tK, sbase + k2::kSK);
+        // descriptors of stage 0 / Q buffer 0 for this group; other stages and
+        // buffers are fixed offsets in the 16-byte address field (no carry: shared
+        // addresses < 256 KB)
+        const uint64_t dQ0 = sdesc_at(tK, qbase + g * 8192), dK0 = sdesc_at(tK, sbase + k2::kSK);
         const uint64_t dV0 = sdesc_at(tV, sbase + k2::kSV);
+        const uint64_t dB0 = sdesc_at(tV, sbase + (g ? k2::kSBb : k2::kSBa)), dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
         constexpr uint64_t kStageStep = k2::kStageBytes >> 4;
         bool ok = true;
-        // S_g(it) = Q_g K(it)^T into buffer it & 1 (head parity qb)
         // S_g(it) = Q_g K(it)^T + Bias_g(it) I into buffer it & 1: the pair bias is
         // added by the tensor core (the staged bias tile is the A operand of four
         // more K-steps against a 64 x 64 identity).
-        const uint64_t dB0 = sdesc_at(tV, sbase + k2::kSBa), dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
-        constexpr uint64_t kBiasStep = (k2::kSBb - k2::kSBa) >> 4;
-        auto issue_s = [&](int g, int it, int qb) {
-            const uint64_t qa = dQ0 + static_cast<uint64_t>(qb * 1024 + g * 512);
+        auto issue_s = [&](int it, int qb) {
             const uint64_t st = static_cast<uint64_t>(it & (k2::kStages - 1));
-            const uint64_t kb = dK0 + st * kStageStep;
-            const uint64_t bb = dB0 + st * kStageStep + static_cast<uint64_t>(g) * kBiasStep;
+            const uint64_t qa = dQ0 + static_cast<uint64_t>(qb * 1024);
+            const uint64_t kb = dK0 + st * kStageStep, bb = dB0 + st * kStageStep;
             const uint32_t d = tmem + k2::colS(g, it & 1);
             mma_ss(d, qa, kb, idS, 0u);
             mma_ss(d, qa + 2, kb + 2, idS, 1u);
@@ -625,83 +628,67 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             for (int kk = 0; kk < k2::kKT / 16; ++kk) mma_ss(d, bb + kk * 2, dI + kk * 2, idS, 1u);
         };
         // O_g (+)= P_g(it) V'(it); the first tile of a head (t == 0) overwrites
-        auto issue_pv = [&](int g, int it, int t) {
+        auto issue_pv = [&](int it, int t) {
             const uint64_t vb = dV0 + static_cast<uint64_t>(it & (k2::kStages - 1)) * kStageStep;
             const uint32_t a = tmem + k2::colS(g, it & 1), d = tmem + k2::colO(g);
             const uint32_t first = t > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < k2::kKT / 16; ++kk) mma_ts(d, a + kk * 8, vb + kk * 2, idO, kk > 0 ? 1u : first);
         };
-        // operands of S(it) present: Q of its head (first tile), K of its stage
+        // operands of S(it) present: Q of its head (first tile), K and bias of its stage
         auto s_ready = [&](int it, int h, int t) -> bool {
             bool r = true;
             if (t == 0) r = mbar_wait(q_full + (h & 1), (h >> 1) & 1, abort);
             if (r) r = mbar_wait(kv_full + (it & (k2::kStages - 1)), (it >> 2) & 1, abort);
             return __all_sync(0xffffffffu, r);
         };
+        auto issue_s_step = [&](int it, int h, int t) {   // leader only
+            tc_fence_after();
+            issue_s(it, h & 1);
+            tc_commit(s_full + g * 2 + (it & 1));
+            if (t == nk - 1) tc_commit(q_empty + (h & 1));   // this group's last read of Q(h)
+        };
         // prologue: S of tiles 0 and 1
         int hn = 0, tn = 0;                           // (head, tile) of the next S to issue
         for (int it = 0; ok && it < 2 && it < NT; ++it) {
             ok = s_ready(it, hn, tn);
             if (!ok) break;
-            if (leader) {
-                tc_fence_after();
-                for (int g = 0; g < 2; ++g) {
-                    issue_s(g, it, hn & 1);
-                    tc_commit(s_full + g * 2 + (it & 1));
-                }
-                if (tn == nk - 1) tc_commit(q_empty + (hn & 1));
-            }
+            if (leader) issue_s_step(it, hn, tn);
             __syncwarp();
             if (++tn == nk) { tn = 0; ++hn; }
         }
         for (int it = 0, tp = 0; ok && it < NT; ++it) {
-            const int nx = it + 2;
-            for (int g = 0; g < 2; ++g) {
-                ok = __all_sync(0xffffffffu, mbar_wait(p_full + g * 2 + (it & 1), (it >> 1) & 1, abort));
-                if (!ok) break;
-                if (leader) {
-                    tc_fence_after();
-                    issue_pv(g, it, tp);
-                    tc_commit(o_ready + g * 2 + (it & 1));
-                    if (g == 1) tc_commit(kv_empty + (it & (k2::kStages - 1)));
-                }
-                if (nx < NT) {
-                    if (g == 0) {
-                        ok = s_ready(nx, hn, tn);
-                        if (!ok) break;
-                    }
-                    if (leader) {
-                        tc_fence_after();
-                        issue_s(g, nx, hn & 1);
-                        tc_commit(s_full + g * 2 + (nx & 1));
-                    }
-                }
-                __syncwarp();
+            ok = __all_sync(0xffffffffu, mbar_wait(p_full + g * 2 + (it & 1), (it >> 1) & 1, abort));
+            if (!ok) break;
+            if (leader) {
+                tc_fence_after();
+                issue_pv(it, tp);
+                tc_commit(o_ready + g * 2 + (it & 1));
+                tc_commit(kv_empty + (it & (k2::kStages - 1)));   // this group is done with the stage
             }
-            if (ok && nx < NT) {
-                if (leader && tn == nk - 1) tc_commit(q_empty + (hn & 1));
+            __syncwarp();
+            const int nx = it + 2;
+            if (nx < NT) {
+                ok = s_ready(nx, hn, tn);
+                if (!ok) break;
+                if (leader) issue_s_step(nx, hn, tn);
+                __syncwarp();
                 if (++tn == nk) { tn = 0; ++hn; }
             }
             if (++tp == nk) tp = 0;
-            __syncwarp();
         }
         if (ok && p.last) {                           // output projection: out = u W_o
             constexpr uint32_t idP = idesc_f16_f32(128, 128);
-            ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, abort));
-            for (int g = 0; ok && g < 2; ++g) {
-                ok = __all_sync(0xffffffffu, mbar_wait(u_full + g, 0, abort));
-                if (!ok) break;
-                if (leader) {
-                    tc_fence_after();
+            ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, abort) && mbar_wait(u_full + g, 0, abort));
+            if (ok && leader) {
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
-                               sdesc_at(tV, qbase + (kk >> 2) * 16384 + (kk & 3) * 32), idP, kk > 0 ? 1u : 0u);
-                    tc_commit(o_full + g);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
+                           sdesc_at(tV, qbase + (kk >> 2) * 16384 + (kk & 3) * 32), idP, kk > 0 ? 1u : 0u);
+                tc_commit(o_full + g);
             }
+            __syncwarp();
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutMma);
     } else if (warp < 4) {
@@ -1049,6 +1036,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.lse_run = W.lse_run ? f32(W.lse_run) : nullptr;
         ap.out = static_cast<__nv_bfloat16*>(a.out);
         ap.status = a.status;
+        ap.inject = k0 == 0 ? a.inject : 0;
         dim3 grid(Ip / 256, I);
         if (tm) tm->begin("sm103_attention", s);
         sm103_attention<<<grid, k2::kThreads, k2::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);

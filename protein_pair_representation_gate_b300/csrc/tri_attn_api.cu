@@ -41,6 +41,7 @@ struct tri_attn_ctx {
         }
     } timer;
     bool timing = false;
+    int inject = 0;          // one-shot test hook
 };
 
 namespace {
@@ -170,6 +171,8 @@ tri_attn_status tri_attn_forward(tri_attn_ctx* c, int node, int I, const void* Z
     a.out = out;
     a.key_chunks = g.key_chunks;
     a.status = c->d_status;
+    a.inject = c->inject;
+    c->inject = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LaunchTimer* t = c->timing ? &c->timer : nullptr;
@@ -191,6 +194,14 @@ tri_attn_status tri_attn_status_sync(tri_attn_ctx* c, void* stream) {
         if (cudaMemset(c->d_status, 0, sizeof v) != cudaSuccess) return TRI_ATTN_ECUDA;
         return TRI_ATTN_ETIMEOUT;
     }
+    return TRI_ATTN_OK;
+}
+
+tri_attn_status tri_attn_debug_inject(tri_attn_ctx* c, int fault) {
+    if (!c) return TRI_ATTN_EINVAL;
+    if (fault != TRI_ATTN_FAULT_NONE && fault != TRI_ATTN_FAULT_SKIP_STAGE) return TRI_ATTN_EINVAL;
+    if (fault != TRI_ATTN_FAULT_NONE && c->path != TRI_ATTN_PATH_SM103) return TRI_ATTN_EUNSUPPORTED;
+    c->inject = fault;
     return TRI_ATTN_OK;
 }
 

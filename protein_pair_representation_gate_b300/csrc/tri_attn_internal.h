@@ -57,6 +57,7 @@ struct FwdArgs {
     void* out;
     int key_chunks;
     uint32_t* status;        // device status word
+    int inject = 0;          // test hook (tri_attn_debug_inject)
 };
 
 // Records an event pair around a launch when timing is on.

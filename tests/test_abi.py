@@ -68,6 +68,7 @@ def test_null_arguments(lib):
     assert lib.tri_attn_status_sync(None, None) == B.EINVAL
     assert lib.tri_attn_set_timing(None, 1) == B.EINVAL
     assert lib.tri_attn_kernel_times(None, None, None, 0) == -1
+    assert lib.tri_attn_debug_inject(None, 1) == B.EINVAL
     lib.tri_attn_destroy(None)
 
 

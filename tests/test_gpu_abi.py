@@ -83,3 +83,33 @@ def test_timing_records_each_kernel(setup):
     assert all(ms > 0 for _, ms in times)
     assert ctx.kernel_times() == []
     assert ctx.status_sync() == B.OK
+
+
+def test_bounded_wait_timeout_is_reported_and_context_recovers(setup):
+    """Failure path without a GPU fault: one block's producer skips a stage load,
+    its bounded waits run out (~2 s), the launch finishes, status_sync reports
+    ETIMEOUT, and the next forward on the same context is correct."""
+    import numpy as np
+    from tests.gpu_cases import assert_close, oracle_out
+    torch, t, ctx, ws = setup
+    out = torch.empty_like(t["Z"])
+    assert ctx.debug_inject(B.FAULT_SKIP_STAGE) == B.OK
+    assert ctx.forward_status(0, 64, t["Z"], t["mask"], t, ws, out) == B.OK
+    assert ctx.status_sync() == B.ETIMEOUT
+    assert ctx.status_sync() == B.OK                     # the word was cleared
+    ctx.forward(0, 64, t["Z"], t["mask"], t, ws, out)
+    assert ctx.status_sync() == B.OK
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert_close(got, oracle_out("evoformer_256", "start", I=64), "bf16", "after recovery")
+
+
+def test_debug_inject_arguments():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    simt = B.TriAttn(B.TriAttnConfig(32, 4, 8, 64, "f32"))
+    assert simt.debug_inject(B.FAULT_SKIP_STAGE) == B.EUNSUPPORTED
+    assert simt.debug_inject(B.FAULT_NONE) == B.OK
+    tc = B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "bf16"))
+    assert tc.debug_inject(7) == B.EINVAL
+    assert tc.debug_inject(B.FAULT_NONE) == B.OK
