@@ -166,6 +166,13 @@ __host__ __device__ __forceinline__ constexpr uint64_t sdesc_tmpl(uint32_t sbo, 
     return (static_cast<uint64_t>(1u) << 16) | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
            (static_cast<uint64_t>(1u) << 46) | (static_cast<uint64_t>(swizzle) << 61);
 }
+// Descriptor of a K-major operand without swizzle: 8-row x 16-byte core
+// matrices, the two K-adjacent core matrices of one K = 16 step `lbo` bytes
+// apart, 8-row groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1u) << 46);
+}
 // descriptor template + start address (16-byte units)
 __device__ __forceinline__ uint64_t sdesc_at(uint64_t tmpl, uint32_t saddr) {
     return tmpl | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
@@ -304,6 +311,14 @@ __device__ __forceinline__ uint32_t exp2_pair_f16x2(float a, float b, float negm
         "cvt.rn.f16x2.f32 h, hi, lo;\n\tex2.approx.f16x2 %0, h;\n\t}"
         : "=r"(r)
         : "f"(a), "f"(b), "f"(negm));
+    return r;
+}
+// f16x2 (2^a, 2^b): round to f16x2, f16x2 exp2 (the max is already subtracted)
+__device__ __forceinline__ uint32_t exp2_pair_f16x2_nosub(float a, float b) {
+    uint32_t r;
+    asm("{\n\t.reg .b32 h;\n\tcvt.rn.f16x2.f32 h, %2, %1;\n\tex2.approx.f16x2 %0, h;\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b));
     return r;
 }
 // same with two f32 exp2 and a rounding pack (more accurate, twice the MUFU work)
