@@ -533,6 +533,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int s = 0; s < k2::kStages; ++s) {
             mbar_init(kv_full + s, 1);
             mbar_init(kv_empty + s, 2);           // one commit per MMA issuer (softmax group)
+        }
+        for (int s = 0; s < 4; ++s) {             // [2 groups][2 buffers or tile parities]
             mbar_init(s_full + s, 1);
             mbar_init(p_full + s, 4);
             mbar_init(o_ready + s, 1);
@@ -681,7 +683,15 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             __syncwarp();
             if (++tn == nk) { tn = 0; ++hn; }
         }
+        // Per tile: P(it) -> P V'(it), then at once S(it+2) into the same buffer (the
+        // tensor core runs one thread's MMAs in order).  The operands of S(it+2) are
+        // checked while P(it) is still being computed, off the P -> S path.
         for (int it = 0, tp = 0; ok && it < NT; ++it) {
+            const int nx = it + 2;
+            if (nx < NT) {
+                ok = s_ready(nx, hn, tn);
+                if (!ok) break;
+            }
             ok = __all_sync(0xffffffffu, mbar_wait(p_full + g * 2 + (it & 1), (it >> 1) & 1, abort));
             if (!ok) break;
             if (leader) {
@@ -689,16 +699,10 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 issue_pv(it, tp);
                 tc_commit(o_ready + g * 2 + (it & 1));
                 tc_commit(kv_empty + (it & (k2::kStages - 1)));   // this group is done with the stage
+                if (nx < NT) issue_s_step(nx, hn, tn);
             }
             __syncwarp();
-            const int nx = it + 2;
-            if (nx < NT) {
-                ok = s_ready(nx, hn, tn);
-                if (!ok) break;
-                if (leader) issue_s_step(nx, hn, tn);
-                __syncwarp();
-                if (++tn == nk) { tn = 0; ++hn; }
-            }
+            if (nx < NT && ++tn == nk) { tn = 0; ++hn; }
             if (++tp == nk) tp = 0;
         }
         if (ok && p.last) {                           // output projection: out = u W_o
@@ -813,38 +817,47 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int k = 0; k < k2::kKT; ++k)
                     if (k >= nvalid) s[k] = -INFINITY;
             }
-            // tile max: four independent 3-input max chains
-            float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
-#pragma unroll
-            for (int k = 4; k < k2::kKT; k += 8) {
-                m0 = max3(m0, s[k], s[k + 1]);
-                m1 = max3(m1, s[k + 2], s[k + 3]);
-                m2 = max3(m2, s[k + 4], s[k + 5]);
-                m3 = max3(m3, s[k + 6], s[k + 7]);
-            }
+            // P V'(it-2) is long complete: observing it every tile keeps the o_ready
+            // phases in step for the waits on P V'(it-1) below.  The test is issued
+            // here and its result used only at the end of the tile.
+            const bool pv2_done = it < 2 || mbar_test(o_ready + g * 2 + b, ((it - 2) >> 1) & 1);
             const float m_used = b ? m_pub1 : m_pub0;
-            const float mt = fmaxf(max3(m0, m1, m2), m3) + m_used;
-            // P V'(it-2) is long complete: waiting for it keeps the o_ready phases in
-            // step at no cost.  P V'(it-1) is waited for only when O is about to be
-            // read: at a head boundary (finalize) or for a rescale, which is rare.
-            // A second wait on that already completed phase (at tile it+1) returns at
-            // once, because P V'(it+1) cannot complete before P(it+1) is written.
-            if (it >= 2 && !mbar_test(o_ready + g * 2 + (it & 1), ((it - 2) >> 1) & 1) &&
-                !mbar_wait(o_ready + g * 2 + (it & 1), ((it - 2) >> 1) & 1, abort)) { ok = false; break; }
-            auto wait_prev_pv = [&]() -> bool {
-                if (!mbar_wait(o_ready + g * 2 + ((it - 1) & 1), ((it - 1) >> 1) & 1, abort)) return false;
-                tc_fence_after();
-                return true;
-            };
-            if (t == 0) {
-                if (it > 0) {
-                    if (!wait_prev_pv()) { ok = false; break; }
-                    finalize(h - 1);
-                }
-                m = round_f16(fminf(fmaxf(mt, kMmin), kMmax));
-            } else {
-                const bool need = mt > m + 8.f;          // rescale only when the max grew by > 2^8
-                if (__any_sync(0xffffffffu, need)) {
+            // Common case: S is already relative to the running max m (m_used == m)
+            // and the head continues, so the exponentials start at once; the tile max,
+            // needed only to detect a rescale, is computed alongside them.
+            const bool fast = t != 0 && __all_sync(0xffffffffu, m_used == m);
+            uint32_t pk[32];
+            if (fast) {
+#pragma unroll
+                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2_nosub(s[k], s[k + 1]);
+            }
+            // tile max (relative to m_used): eight independent 3-input max chains
+            float mx[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = max3(s[c], s[8 + c], s[16 + c]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[24 + c], s[32 + c]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[40 + c], s[48 + c]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], s[56 + c]);
+            const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) + m_used;
+            const bool need = mt > m + 8.f;              // rescale only when the max grew by > 2^8
+            const bool redo = t == 0 || __any_sync(0xffffffffu, need);
+            if (!fast || redo) {
+                if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) { ok = false; break; }
+                auto wait_prev_pv = [&]() -> bool {
+                    if (!mbar_wait(o_ready + g * 2 + (b ^ 1), ((it - 1) >> 1) & 1, abort)) return false;
+                    tc_fence_after();
+                    return true;
+                };
+                if (t == 0) {
+                    if (it > 0) {
+                        if (!wait_prev_pv()) { ok = false; break; }
+                        finalize(h - 1);
+                    }
+                    m = round_f16(fminf(fmaxf(mt, kMmin), kMmax));
+                } else if (redo) {
                     if (!wait_prev_pv()) { ok = false; break; }
                     uint32_t ov[32];
                     tmem_ld32(tO, ov);
@@ -859,15 +872,12 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     tmem_st1(tO + 32, lv);
                     m = mn;
                 }
-            }
-            uint32_t pk[32];
-            if (__all_sync(0xffffffffu, m_used == m)) {  // S already relative to m: the common case
-#pragma unroll
-                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2_nosub(s[k], s[k + 1]);
-            } else {                                      // head start or rescale since S was issued
                 const float dm = m_used - m;
 #pragma unroll
                 for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], dm);
+            } else if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) {
+                ok = false;
+                break;
             }
             tmem_st32(tS, pk);
             // publish m for S(it + 2) (issued after this tile's p_full arrive)
