@@ -166,24 +166,31 @@ struct ProjParams {
 };
 
 namespace k1 {
-constexpr int kThreads = 320;                // 2 epilogue warpgroups + producer warp + MMA warp
+constexpr int kThreads = 576;                // 4 epilogue warpgroups + producer warp + MMA warp
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
 constexpr int kW = 0;                        // 4 x 32 KB: [half(qk|vg)][k-half][256 rows][128 B]
 constexpr int kZ = 131072;                   // 2 stages x 32 KB: [k-half][128 rows][128 B]
 constexpr int kConst = kZ + 2 * 32768;       // cst[256][4], wb32[128][4], bias colsum[4], bias offset[4]
 constexpr int kConstBytes = (256 * 4 + CZ * NH + 2 * NH) * 4;
 constexpr int kBar = kConst + ((kConstBytes + 127) / 128) * 128;
-constexpr int kSmem = kBar + 256 + 1024;     // + alignment slack
+// Output staging for the TMA stores of q, k and g: one 32-row x 64-byte box (64-byte
+// swizzle) per warp of those three warpgroups.
+constexpr int kStg = ((kBar + 256 + 1023) / 1024) * 1024;
+constexpr int kStgWarp = 2048;
+constexpr int kSmem = kStg + 12 * kStgWarp + 1024;   // + alignment slack
+static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
 }  // namespace k1
 
 __global__ void __launch_bounds__(k1::kThreads, 1)
 sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__ CUtensorMap mapZe,
-              const __grid_constant__ CUtensorMap mapW, ProjParams p) {
+              const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapQs,
+              const __grid_constant__ CUtensorMap mapKs, const __grid_constant__ CUtensorMap mapGs, ProjParams p) {
     extern __shared__ uint8_t smem_raw[];
     if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* s_cst = reinterpret_cast<float*>(sm + k1::kConst);   // [256][4]
-    float* s_wb = s_cst + 256 * 4;         // [128][4]
-    float* s_bcs = s_wb + CZ * NH;         // [4] pair-bias column sums
+    float* s_wbt = s_cst + 256 * 4;        // [4 heads][128 channels]: (gamma . W_b)^T
+    float* s_bcs = s_wbt + CZ * NH;        // [4] pair-bias column sums
     float* s_bbw = s_bcs + NH;             // [4] pair-bias beta W
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k1::kBar);
     uint64_t* w_full = bars + 0;
@@ -196,7 +203,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < 256 * 4; i += blockDim.x) s_cst[i] = p.cst[i];
-    for (int i = threadIdx.x; i < CZ * NH; i += blockDim.x) s_wb[i] = p.wb32[i];
+    for (int i = threadIdx.x; i < CZ * NH; i += blockDim.x) s_wbt[(i % NH) * CZ + i / NH] = p.wb32[i];
     if (threadIdx.x < NH) {
         s_bcs[threadIdx.x] = p.colsum[NPROJ + threadIdx.x];
         s_bbw[threadIdx.x] = p.betaw[NPROJ + threadIdx.x];
@@ -205,14 +212,14 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
         mbar_init(w_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(z_full + s, 1);
-            mbar_init(z_empty + s, 1 + 8);
+            mbar_init(z_empty + s, 1 + 16);       // MMA commit + 16 epilogue warps
             mbar_init(acc_full + s, 1);
-            mbar_init(acc_empty + s, 4);
+            mbar_init(acc_empty + s, 8);          // the two warpgroups reading this half
         }
         *abort = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == k1::kMmaWarp) {
         tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
@@ -221,7 +228,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 8) {
+    if (warp == k1::kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&mapZs);
@@ -249,7 +256,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == k1::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 256);
@@ -278,11 +285,15 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ epilogue warpgroups
-        const int wg = warp >> 2;                // 0: q, v   1: k, g + pair bias
+        // Warpgroup w owns accumulator columns 128 w .. 128 w + 127, i.e. projection
+        // group w (q, v, k, g), and the pair bias of head w.
+        const int wg = warp >> 2;
         const int wq = warp & 3;                 // TMEM lane quarter
         const int r = wq * 32 + lane;            // row = pair within the tile
-        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wg * 256;
-        const float qscale = kLog2e * rsqrtf((float)HD);
+        const int half = wg >> 1;                // accumulator half (q|v or k|g)
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + wg * 128;
+        const float* wbt = s_wbt + wg * CZ;
+        uint8_t* stg = sm + k1::kStg + ((wg == kGroupQ ? 0 : wg - 1) * 4 + wq) * k1::kStgWarp;   // unused by v
         int j = 0;
         for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x, ++j) {
             const int s = j & 1;
@@ -293,32 +304,26 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
             }
             // LayerNorm statistics of the raw pair vector in one pass over its SMEM row,
             // shifted by its first channel (exact algebra; avoids cancellation when
-            // the mean is large against the spread).  The pair-bias group also
-            // accumulates z . (gamma W_b)[:, h] for its four heads in the same pass.
+            // the mean is large against the spread), and z . (gamma W_b)[:, wg] for
+            // this warpgroup's head in the same pass.
             const uint8_t* zb = sm + k1::kZ + s * 32768 + r * 128;
             const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(zb + ((0 ^ (r & 7)) << 4)));
-            float sd = 0.f, sq = 0.f;
-            float bh0 = 0.f, bh1 = 0.f, bh2 = 0.f, bh3 = 0.f;
+            float sd = 0.f, sq = 0.f, bh = 0.f;
 #pragma unroll 2
             for (int cc = 0; cc < 16; ++cc) {
                 const int b = cc >> 3, c = cc & 7;
                 const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
+                const float4 wa = *reinterpret_cast<const float4*>(wbt + cc * 8);
+                const float4 wb = *reinterpret_cast<const float4*>(wbt + cc * 8 + 4);
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                     const float z0 = bf16lo(w4[q2]), z1 = bf16hi(w4[q2]);
                     const float d0 = z0 - shift, d1 = z1 - shift;
                     sd += d0 + d1;
                     sq = fmaf(d0, d0, fmaf(d1, d1, sq));
-                    if (wg == 1) {
-                        const int ch = cc * 8 + q2 * 2;
-                        const float4 w0 = *reinterpret_cast<const float4*>(s_wb + ch * NH);
-                        const float4 w1 = *reinterpret_cast<const float4*>(s_wb + (ch + 1) * NH);
-                        bh0 = fmaf(z0, w0.x, fmaf(z1, w1.x, bh0));
-                        bh1 = fmaf(z0, w0.y, fmaf(z1, w1.y, bh1));
-                        bh2 = fmaf(z0, w0.z, fmaf(z1, w1.z, bh2));
-                        bh3 = fmaf(z0, w0.w, fmaf(z1, w1.w, bh3));
-                    }
+                    bh = fmaf(z0, wv[2 * q2], fmaf(z1, wv[2 * q2 + 1], bh));
                 }
             }
             __syncwarp();
@@ -327,34 +332,29 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
             const float mu = shift + md;
             const float var = fmaxf(sq * (1.f / CZ) - md * md, 0.f);
             const float rstd = rsqrtf(var + p.eps);
-            const float nmr = -mu * rstd;
-
-            if (wg == 1) {
-                // pair bias: b_h = rstd * (z . gW_b[:, h] - mu * colsum) + beta W_b, in log2 units
+            {
+                // pair bias of head wg: rstd * (z . gW_b[:, h] - mu * colsum) + beta W_b, in log2 units
                 const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
-                const float bh[NH] = {bh0, bh1, bh2, bh3};
-#pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    const float v = (fmaf(bh[h], rstd, nmr * s_bcs[h]) + s_bbw[h]) * kLog2e;
-                    p.bias[((size_t)h * p.I_pad + L) * p.I_pad + x] = __float2half_rn(valid ? v : kMaskedBias);
-                }
+                const float v = (fmaf(bh, rstd, -mu * rstd * s_bcs[wg]) + s_bbw[wg]) * kLog2e;
+                p.bias[((size_t)wg * p.I_pad + L) * p.I_pad + x] = __float2half_rn(valid ? v : kMaskedBias);
             }
 
-            if (!mbar_wait(acc_full + wg, j & 1, abort)) {
+            if (!mbar_wait(acc_full + half, j & 1, abort)) {
                 set_abort(abort, p.status, kStatusTimeoutEpilogue);
                 break;
             }
             tc_fence_after();
-            // 32 accumulator columns -> normalised, transformed f16 values -> global.
-            // value = r * (acc - mu * colsum) + off, two columns per packed FMA, with
-            // r = rstd (times log2(e)/sqrt(d) for q) and off from the prepared constants.
-            const float rq = rstd * (kLog2e * rsqrtf((float)HD));
+            // 32 accumulator columns (one head) -> normalised, transformed f16 values ->
+            // global.  value = r * (acc - mu * colsum) + off, two columns per packed FMA,
+            // with r = rstd (times log2(e)/sqrt(d) for q) and off from the prepared constants.
+            const float rr = wg == kGroupQ ? rstd * (kLog2e * rsqrtf((float)HD)) : rstd;
             const float nmu = -mu;
-            auto emit = [&](int cb, const uint32_t (&acc)[32]) {
-                const int n0 = wg * 256 + cb * 32;
-                const int which = n0 / CH, h = (n0 % CH) / HD;
-                const float rr = which == kGroupQ ? rq : rstd;
-                const float4* cst = reinterpret_cast<const float4*>(s_cst) + (n0 >> 1);
+#pragma unroll 1
+            for (int h = 0; h < NH; ++h) {
+                uint32_t acc[32];
+                tmem_ld32(tl + h * 32, acc);
+                tmem_ld_wait();
+                const float4* cst = reinterpret_cast<const float4*>(s_cst) + ((wg * 128 + h * 32) >> 1);
                 uint32_t o[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
@@ -362,18 +362,14 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                     float t0, t1, v0, v1;
                     fma2(t0, t1, nmu, nmu, c.x, c.y, __uint_as_float(acc[e]), __uint_as_float(acc[e + 1]));
                     fma2(v0, v1, rr, rr, t0, t1, c.z, c.w);
-                    if (which == kGroupG) {               // sigmoid(v) = 0.5 tanh(v / 2) + 0.5
+                    if (wg == kGroupG) {                  // sigmoid(v) = 0.5 tanh(v / 2) + 0.5
                         v0 = fmaf(0.5f, tanh_approx(0.5f * v0), 0.5f);
                         v1 = fmaf(0.5f, tanh_approx(0.5f * v1), 0.5f);
                     }
                     o[e >> 1] = pack_f16(v0, v1);
                 }
                 const size_t lh = (size_t)L * NH + h;
-                if (which == kGroupG) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + h * HD);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                } else if (which == kGroupV) {
+                if (wg == kGroupV) {
                     unsigned short* dst = reinterpret_cast<unsigned short*>(p.vt + lh * HD * p.I_pad + x);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -381,29 +377,34 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                         dst[(size_t)(e + 1) * p.I_pad] = static_cast<unsigned short>(o[e >> 1] >> 16);
                     }
                 } else {
-                    __half* base = which == kGroupQ ? p.q : p.k;
-                    uint4* dst = reinterpret_cast<uint4*>(base + (lh * p.I_pad + x) * HD);
+                    // q, k, g rows of head h: [line * 4 + h][x][32], written through this
+                    // warp's staging box (row lane, 16-byte chunk c at c ^ ((lane >> 1) & 3))
+                    // and one TMA store.  The box is rewritten only after the previous
+                    // store has read it.
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                            make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const CUtensorMap* m = wg == kGroupQ ? &mapQs : (wg == kGroupK ? &mapKs : &mapGs);
+                        tma_store_2d(m, stg, 0, static_cast<int>(lh * p.I_pad) + x - lane);
+                        bulk_commit();
+                    }
                 }
-            };
-#pragma unroll 1
-            for (int cb = 0; cb < 8; cb += 2) {          // two TMEM loads in flight per wait
-                uint32_t acc0[32], acc1[32];
-                tmem_ld32(tl + cb * 32, acc0);
-                tmem_ld32(tl + cb * 32 + 32, acc1);
-                tmem_ld_wait();
-                emit(cb, acc0);
-                emit(cb + 1, acc1);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + wg);
+            if (lane == 0) mbar_arrive(acc_empty + half);
         }
+        if (lane == 0) bulk_wait0();              // this warp's stores complete before exit
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == k1::kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -776,7 +777,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int e4 = 0; e4 < HD / 4; ++e4)
                     orun[e4] = make_float4(o[4 * e4], o[4 * e4 + 1], o[4 * e4 + 2], o[4 * e4 + 3]);
             } else {
-                const uint4* gp = reinterpret_cast<const uint4*>(p.g + ((size_t)L * p.I_pad + x) * CH + hp * HD);
+                const uint4* gp = reinterpret_cast<const uint4*>(p.g + (((size_t)L * NH + hp) * p.I_pad + x) * HD);
                 uint32_t u[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -1037,6 +1038,12 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     if (!map3d(&mZs, a.Z, CZ, I, I, zrow, zline, 64, 128, 1) || !map3d(&mZe, a.Z, CZ, I, I, zrow, zline, 64, 1, 128) ||
         !map2d(&mW, bf(W.wprep), CZ, NPROJ, CZ * 2, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return cudaErrorInvalidValue;
+    CUtensorMap mQs, mKs, mGs;
+    const uint64_t rows_lh = (uint64_t)I * NH * Ip;
+    if (!map2d(&mQs, hf(W.q), HD, rows_lh, HD * 2, HD, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mKs, hf(W.k), HD, rows_lh, HD * 2, HD, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mGs, hf(W.g), HD, rows_lh, HD * 2, HD, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     ProjParams pp;
     pp.node = a.node;
     pp.I = I;
@@ -1058,7 +1065,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     {
         const int grid = pp.ntiles < num_sms() ? pp.ntiles : num_sms();
         if (tm) tm->begin("sm103_ln_proj", s);
-        sm103_ln_proj<<<grid, k1::kThreads, k1::kSmem, s>>>(mZs, mZe, mW, pp);
+        sm103_ln_proj<<<grid, k1::kThreads, k1::kSmem, s>>>(mZs, mZe, mW, mQs, mKs, mGs, pp);
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
