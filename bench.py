@@ -42,6 +42,26 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM traffic of one sm103_attention launch, from one ncu capture of dram__bytes_read.sum +
+# dram__bytes_write.sum at I=512 (start node: 271.0 MB read + 48.3 MB written; summary in
+# profiles/dram_traffic_complex_2048_I512.md), scaled to I=2048 by the pair count (x16): the kernel's
+# operand traffic (q, k, vT, g, bias, out) grows with I^2.  Valid only for the kernel sources it was
+# captured with (hash below); any change to them reports null until the capture is repeated.
+ATTN_TRAFFIC_I512 = 271.0e6 + 48.3e6
+ATTN_TRAFFIC_SRC = "3f066071be967cdc"
+
+
+def attention_traffic(I: int):
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("sm103_kernels.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "protein_pair_representation_gate_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != ATTN_TRAFFIC_SRC:
+        return None
+    return ATTN_TRAFFIC_I512 * (I / 512) ** 2
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -286,7 +306,8 @@ def main():
         ach = per_launch_flops / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "peak_source": f"{src} bf16 burst", "frac_of_sustained":
-                (ach / peak_sus if peak_sus else None), "traffic": None}
+                (ach / peak_sus if peak_sus else None), "traffic": attention_traffic(wl.I),
+                "traffic_unit": "bytes per launch (ncu at I=512, scaled by I^2)"}
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     e2e = None
