@@ -68,11 +68,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // if every key so far was masked, the first real key's rescale factor 2^-30000
 // removes their contribution exactly).
 constexpr float kMaskedBias = -30000.f;
-// Range of the attention kernel's running max (log2 units).  The max is held at
-// f16-representable values because the tensor core subtracts it from S as an
-// f16 operand; both bounds are exact in f16.
-constexpr float kMmin = -60000.f, kMmax = 60000.f;
-__device__ __forceinline__ float round_f16(float x) { return __half2float(__float2half_rn(x)); }
+constexpr float kMfloor = -1e30f;           // finite floor of the attention kernel's running max
 
 // Block-uniform read of the device status word (one thread reads, all see the
 // same value), so an early return never splits a block at a later barrier.
@@ -428,7 +424,7 @@ namespace k2 {
 constexpr int kThreads = 384;                // control warpgroup (producer, 2 MMA issuers, 1 idle) + 2 softmax warpgroups
 constexpr int kKT = 64;                      // keys per stage (one S sub-tile)
 constexpr int kStages = 4;                  // power of two: stage = it & 3, phase = (it >> 2) & 1
-constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64); W_o at the end
+constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64)
 constexpr int kStage = 32768;
 constexpr int kSK = 0;                       // K tile: 64 keys x 64 B (SW64)
 constexpr int kSV = 4096;                    // V' tile: 32 rows V^T + 16 rows [1; 0], 128 B each (SW128)
@@ -436,10 +432,7 @@ constexpr int kSBa = 10240, kSBb = 26624;    // bias tiles of the two query tile
 constexpr int kStageBytes = 43008;
 constexpr int kStageTx = 4096 + 4096 + 32768;   // bytes the TMA writes per stage
 constexpr int kIdent = kStage + kStages * kStageBytes;   // 64 x 64 f16 identity (SW128, K-major)
-constexpr int kMt = kIdent + 8192;           // [2 groups][2 bufs] 128 rows x 16 B: the row's -m (no swizzle)
-constexpr int kEt = kMt + 4 * 2048;          // 64 rows x 16 B: 1.0 in column 0 (no swizzle)
-constexpr int kZt = kEt + 1024;              // 128 rows x 16 B of zeros: columns 8..15 of both
-constexpr int kBar = kZt + 2048;
+constexpr int kBar = kIdent + 8192;
 constexpr int kSmem = kBar + 512 + 1024;     // barriers + alignment slack
 // TMEM columns
 __host__ __device__ constexpr uint32_t colS(int g, int b) { return g * 128u + b * 64u; }   // S / P buffers
@@ -510,15 +503,6 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             w[e >> 1] = (e & 1) ? 0x3C000000u : 0x00003C00u;
         }
         *reinterpret_cast<uint4*>(sm + k2::kIdent + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    // The row max enters S through one more K-step, S' = S - m = ... + M E^T:
-    // M (128 x 16, one per group and S buffer) holds -m of each query row in
-    // column 0, E (64 x 16) holds 1.0 in column 0, and columns 8..15 of both
-    // are one shared block of zeros.  M starts at 0.
-    for (int i = threadIdx.x; i < (k2::kBar - k2::kMt) / 16; i += blockDim.x) {
-        const int off = k2::kMt + i * 16;
-        const uint32_t w0 = (off >= k2::kEt && off < k2::kZt) ? 0x00003C00u : 0u;
-        *reinterpret_cast<uint4*>(sm + off) = make_uint4(w0, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
 
@@ -633,26 +617,23 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const uint64_t dQ0 = sdesc_at(tK, qbase + g * 8192), dK0 = sdesc_at(tK, sbase + k2::kSK);
         const uint64_t dV0 = sdesc_at(tV, sbase + k2::kSV);
         const uint64_t dB0 = sdesc_at(tV, sbase + (g ? k2::kSBb : k2::kSBa)), dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
-        const uint32_t mbase = smem_u32(sm + k2::kMt + g * 4096);
-        const uint64_t dM0 = sdesc_noswizzle(mbase, k2::kZt - k2::kMt - g * 4096, 128);
-        const uint64_t dM1 = sdesc_noswizzle(mbase + 2048, k2::kZt - k2::kMt - g * 4096 - 2048, 128);
-        const uint64_t dE = sdesc_noswizzle(smem_u32(sm + k2::kEt), k2::kZt - k2::kEt, 128);
         constexpr uint64_t kStageStep = k2::kStageBytes >> 4;
         bool ok = true;
-        // S'_g(it) = Q_g K(it)^T + Bias_g(it) I - m into buffer it & 1: the pair bias
-        // (the staged bias tile as the A operand of four K-steps against a 64 x 64
-        // identity) and the row max the group last published (one K-step) are
-        // applied by the tensor core.
-        auto issue_s = [&](int it, int qb) {
+        // S_g(it) = Q_g K(it)^T + Bias_g(it) I into buffer it & 1: the pair bias is
+        // added by the tensor core (the staged bias tile is the A operand of four
+        // more K-steps against a 64 x 64 identity).
+        // Q_g of head h is copied once from its staged tile into TMEM columns
+        // colU(g) + 16 h .. + 15 (free until the head's gated output is written there
+        // at the start of the next head), and Q K^T reads its A operand from TMEM.
+        auto issue_s = [&](int it, int h) {
             const uint64_t st = static_cast<uint64_t>(it & (k2::kStages - 1));
-            const uint64_t qa = dQ0 + static_cast<uint64_t>(qb * 1024);
+            const uint32_t qt = tmem + k2::colU(g) + h * 16;
             const uint64_t kb = dK0 + st * kStageStep, bb = dB0 + st * kStageStep;
             const uint32_t d = tmem + k2::colS(g, it & 1);
-            mma_ss(d, qa, kb, idS, 0u);
-            mma_ss(d, qa + 2, kb + 2, idS, 1u);
+            mma_ts(d, qt, kb, idS, 0u);
+            mma_ts(d, qt + 8, kb + 2, idS, 1u);
 #pragma unroll
             for (int kk = 0; kk < k2::kKT / 16; ++kk) mma_ss(d, bb + kk * 2, dI + kk * 2, idS, 1u);
-            mma_ss(d, (it & 1) ? dM1 : dM0, dE, idS, 1u);   // - the row max the group published for it
         };
         // O_g (+)= P_g(it) V'(it); the first tile of a head (t == 0) overwrites
         auto issue_pv = [&](int it, int t) {
@@ -671,9 +652,15 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         };
         auto issue_s_step = [&](int it, int h, int t) {   // leader only
             tc_fence_after();
-            issue_s(it, h & 1);
+            if (t == 0) {                                     // Q(h): smem -> TMEM, then release the buffer
+                const uint64_t qa = dQ0 + static_cast<uint64_t>((h & 1) * 1024);
+                const uint32_t qt = tmem + k2::colU(g) + h * 16;
+                tmem_cp_128x256b(qt, qa);
+                tmem_cp_128x256b(qt + 8, qa + 2);
+                tc_commit(q_empty + (h & 1));
+            }
+            issue_s(it, h);
             tc_commit(s_full + g * 2 + (it & 1));
-            if (t == nk - 1) tc_commit(q_empty + (h & 1));   // this group's last read of Q(h)
         };
         // prologue: S of tiles 0 and 1
         int hn = 0, tn = 0;                           // (head, tile) of the next S to issue
@@ -731,13 +718,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int x = xq0 + g * 128 + r;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tO = tl + k2::colO(g), tU = tl + k2::colU(g);
-        // Running max m (log2 units), kept at f16-representable values so that the
-        // tensor core subtracts exactly m.  m_pub0 / m_pub1 are the values in the -m
-        // tiles of S buffers 0 / 1: the ones S(it) used.  The tile of buffer b is rewritten at tile
-        // it (for S(it + 2)) only after S(it) has completed.
-        float m = kMmin;
-        float m_pub0 = 0.f, m_pub1 = 0.f;
-        uint8_t* const mrow = sm + k2::kMt + g * 4096 + r * 16;
+        float m = kMfloor;                        // running max (log2 units)
         bool ok = true;
 
         // normalise head hp, merge with the running chunk state, gate into u (TMEM)
@@ -798,7 +779,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const uint32_t tS = tl + k2::colS(g, b);
             if (!mbar_wait(s_full + g * 2 + b, (it >> 1) & 1, abort)) { ok = false; break; }
             tc_fence_after();
-            // ---- scores of key tile it, S - m_used (bias and -m_used added by the tensor core)
+            // ---- scores of key tile it (bias already added by the tensor core)
             float s[k2::kKT];
             {
                 uint32_t va[32], vb[32];
@@ -822,17 +803,17 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             // phases in step for the waits on P V'(it-1) below.  The test is issued
             // here and its result used only at the end of the tile.
             const bool pv2_done = it < 2 || mbar_test(o_ready + g * 2 + b, ((it - 2) >> 1) & 1);
-            const float m_used = b ? m_pub1 : m_pub0;
-            // Common case: S is already relative to the running max m (m_used == m)
-            // and the head continues, so the exponentials start at once; the tile max,
-            // needed only to detect a rescale, is computed alongside them.
-            const bool fast = t != 0 && __all_sync(0xffffffffu, m_used == m);
+            // Common case (the head continues): the exponentials against the running max
+            // start at once; the tile max, needed only to detect a rescale, is computed
+            // alongside them.
+            const bool fast = t != 0;
             uint32_t pk[32];
             if (fast) {
+                const float negm = -m;
 #pragma unroll
-                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2_nosub(s[k], s[k + 1]);
+                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
             }
-            // tile max (relative to m_used): eight independent 3-input max chains
+            // tile max: eight independent 3-input max chains
             float mx[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) mx[c] = max3(s[c], s[8 + c], s[16 + c]);
@@ -842,7 +823,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[40 + c], s[48 + c]);
 #pragma unroll
             for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], s[56 + c]);
-            const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) + m_used;
+            const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             const bool need = mt > m + 8.f;              // rescale only when the max grew by > 2^8
             const bool redo = t == 0 || __any_sync(0xffffffffu, need);
             if (!fast || redo) {
@@ -857,14 +838,14 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         if (!wait_prev_pv()) { ok = false; break; }
                         finalize(h - 1);
                     }
-                    m = round_f16(fminf(fmaxf(mt, kMmin), kMmax));
+                    m = fmaxf(mt, kMfloor);
                 } else if (redo) {
                     if (!wait_prev_pv()) { ok = false; break; }
                     uint32_t ov[32];
                     tmem_ld32(tO, ov);
                     uint32_t lv = tmem_ld1(tO + 32);
                     tmem_ld_wait();
-                    const float mn = need ? round_f16(fminf(mt, kMmax)) : m;
+                    const float mn = need ? mt : m;
                     const float alpha = ex2(m - mn);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
@@ -873,23 +854,14 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     tmem_st1(tO + 32, lv);
                     m = mn;
                 }
-                const float dm = m_used - m;
+                const float negm = -m;
 #pragma unroll
-                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], dm);
+                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
             } else if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) {
                 ok = false;
                 break;
             }
             tmem_st32(tS, pk);
-            // publish m for S(it + 2) (issued after this tile's p_full arrive)
-            const bool pub = m != m_used;
-            if (__any_sync(0xffffffffu, pub)) {
-                if (pub) {
-                    *reinterpret_cast<__half*>(mrow + b * 2048) = __float2half_rn(-m);
-                    if (b) m_pub1 = m; else m_pub0 = m;
-                }
-                fence_proxy_async_smem();
-            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

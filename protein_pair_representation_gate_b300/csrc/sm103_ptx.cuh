@@ -142,6 +142,12 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// Copy a 128-row x 32-byte operand tile (described like an MMA operand) from shared
+// memory to TMEM: row i -> lane i, its 32 bytes -> 8 consecutive columns.  Ordered
+// with this thread's later tcgen05.mma instructions.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // D[tmem] (+)= A[tmem] * B[smem]^T
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -176,13 +182,6 @@ constexpr uint32_t kSwizzle64 = 4;
 __host__ __device__ __forceinline__ constexpr uint64_t sdesc_tmpl(uint32_t sbo, uint32_t swizzle) {
     return (static_cast<uint64_t>(1u) << 16) | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
            (static_cast<uint64_t>(1u) << 46) | (static_cast<uint64_t>(swizzle) << 61);
-}
-// Descriptor of a K-major operand without swizzle: 8-row x 16-byte core
-// matrices, the two K-adjacent core matrices of one K = 16 step `lbo` bytes
-// apart, 8-row groups `sbo` bytes apart.
-__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1u) << 46);
 }
 // descriptor template + start address (16-byte units)
 __device__ __forceinline__ uint64_t sdesc_at(uint64_t tmpl, uint32_t saddr) {
@@ -322,14 +321,6 @@ __device__ __forceinline__ uint32_t exp2_pair_f16x2(float a, float b, float negm
         "cvt.rn.f16x2.f32 h, hi, lo;\n\tex2.approx.f16x2 %0, h;\n\t}"
         : "=r"(r)
         : "f"(a), "f"(b), "f"(negm));
-    return r;
-}
-// f16x2 (2^a, 2^b): round to f16x2, f16x2 exp2 (the max is already subtracted)
-__device__ __forceinline__ uint32_t exp2_pair_f16x2_nosub(float a, float b) {
-    uint32_t r;
-    asm("{\n\t.reg .b32 h;\n\tcvt.rn.f16x2.f32 h, %2, %1;\n\tex2.approx.f16x2 %0, h;\n\t}"
-        : "=r"(r)
-        : "f"(a), "f"(b));
     return r;
 }
 // same with two f32 exp2 and a rounding pack (more accurate, twice the MUFU work)
