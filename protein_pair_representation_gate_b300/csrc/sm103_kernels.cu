@@ -722,6 +722,14 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         bool ok = true;
 
         // normalise head hp, merge with the running chunk state, gate into u (TMEM)
+        // gate of the head being finished, loaded at the head's last tile so that its
+        // global-memory latency is hidden (heads of one tile load it in finalize)
+        uint4 gpre[4];
+        auto load_gate = [&](int hh) {
+            const uint4* gp = reinterpret_cast<const uint4*>(p.g + (((size_t)L * NH + hh) * p.I_pad + x) * HD);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gpre[i] = gp[i];
+        };
         auto finalize = [&](int hp) {
             uint32_t ov[32];
             tmem_ld32(tO, ov);
@@ -758,11 +766,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int e4 = 0; e4 < HD / 4; ++e4)
                     orun[e4] = make_float4(o[4 * e4], o[4 * e4 + 1], o[4 * e4 + 2], o[4 * e4 + 3]);
             } else {
-                const uint4* gp = reinterpret_cast<const uint4*>(p.g + (((size_t)L * NH + hp) * p.I_pad + x) * HD);
+                if (nk == 1) load_gate(hp);
                 uint32_t u[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 gv = gp[i];
+                    const uint4 gv = gpre[i];
                     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -777,6 +785,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int it = 0, h = 0, t = 0; it < NT; ++it, t = (t + 1 == nk) ? 0 : t + 1, h += (t == 0) ? 1 : 0) {
             const int b = it & 1;
             const uint32_t tS = tl + k2::colS(g, b);
+            if (nk > 1 && t == nk - 1 && p.last) load_gate(h);
             if (!mbar_wait(s_full + g * 2 + b, (it >> 1) & 1, abort)) { ok = false; break; }
             tc_fence_after();
             // ---- scores of key tile it (bias already added by the tensor core)
