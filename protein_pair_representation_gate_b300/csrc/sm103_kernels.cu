@@ -423,22 +423,29 @@ struct AttnParams {
 namespace k2 {
 constexpr int kThreads = 384;                // control warpgroup (producer, 2 MMA issuers, 1 idle) + 2 softmax warpgroups
 constexpr int kKT = 64;                      // keys per stage (one S sub-tile)
-constexpr int kStages = 4;                  // power of two: stage = it & 3, phase = (it >> 2) & 1
+// K and V' of a key tile live in a ring shared by both groups (freed when both
+// groups' P V' has read it); each group's bias tiles live in a ring of its own,
+// freed as soon as that group's S has read it, so the groups do not hold each
+// other's loads back.
+constexpr int kStages = 5;                   // K / V' ring: stage = it % 5, phase = (it / 5) & 1
+constexpr int kBStages = 4;                  // bias ring per group: it & 3, phase (it >> 2) & 1
 constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64)
 constexpr int kStage = 32768;
 constexpr int kSK = 0;                       // K tile: 64 keys x 64 B (SW64)
 constexpr int kSV = 4096;                    // V' tile: 32 rows V^T + 16 rows [1; 0], 128 B each (SW128)
-constexpr int kSBa = 10240, kSBb = 26624;    // bias tiles of the two query tiles: 128 rows x 128 B (SW128)
-constexpr int kStageBytes = 43008;
-constexpr int kStageTx = 4096 + 4096 + 32768;   // bytes the TMA writes per stage
-constexpr int kIdent = kStage + kStages * kStageBytes;   // 64 x 64 f16 identity (SW128, K-major)
+constexpr int kStageBytes = 10240;
+constexpr int kStageTx = 4096 + 4096;        // bytes the TMA writes per K / V' stage
+constexpr int kBias = kStage + kStages * kStageBytes;    // [2 groups][4] bias tiles: 128 rows x 128 B (SW128)
+constexpr int kBiasBytes = 16384;
+constexpr int kIdent = kBias + 2 * kBStages * kBiasBytes;   // 64 x 64 f16 identity (SW128, K-major)
 constexpr int kBar = kIdent + 8192;
 constexpr int kSmem = kBar + 512 + 1024;     // barriers + alignment slack
 // TMEM columns
 __host__ __device__ constexpr uint32_t colS(int g, int b) { return g * 128u + b * 64u; }   // S / P buffers
 __host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 64u; }  // O (32) | row sum l (1)
 __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  // gated u (f16 pairs)
-static_assert(kStages == 4, "stage index and phase are computed with it & 3 and (it >> 2) & 1");
+static_assert(kBStages == 4, "bias stage index and phase are computed with it & 3 and (it >> 2) & 1");
+static_assert(kBias % 1024 == 0 && kIdent % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
 }  // namespace k2
 
@@ -470,8 +477,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k2::kBar);
     uint64_t* q_full = bars + 0;      // [2]
     uint64_t* q_empty = bars + 2;     // [2]
-    uint64_t* kv_full = bars + 4;     // [4]
-    uint64_t* kv_empty = bars + 8;    // [4]
+    uint64_t* kv_full = bars + 48;    // [5]
+    uint64_t* kv_empty = bars + 56;   // [5]
     uint64_t* s_full = bars + 12;     // [2 groups][2 buffers]
     // P and O barriers alternate by tile parity: with two S buffers a softmax group
     // can write P(it) and P(it+1) before the MMA warp has waited for P(it), and one
@@ -483,6 +490,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     uint64_t* w_full = bars + 28;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 29);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 30);
+    uint64_t* b_full = bars + 32;     // [2 groups][4]: bias tile staged
+    uint64_t* b_empty = bars + 40;    // [2 groups][4]: S of that tile done (bias read)
 
     // Rows 32..47 of each stage's V': a row of ones (gives the softmax row sum as
     // output column 32 of P V') and 15 zero rows.  Same in every swizzle phase.
@@ -518,6 +527,10 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int s = 0; s < k2::kStages; ++s) {
             mbar_init(kv_full + s, 1);
             mbar_init(kv_empty + s, 2);           // one commit per MMA issuer (softmax group)
+        }
+        for (int s = 0; s < 2 * k2::kBStages; ++s) {
+            mbar_init(b_full + s, 1);
+            mbar_init(b_empty + s, 1);            // the group's MMA issuer commits after S
         }
         for (int s = 0; s < 4; ++s) {             // [2 groups][2 buffers or tile parities]
             mbar_init(s_full + s, 1);
@@ -559,7 +572,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int h = 0, it = 0; ok && h < NH; ++h) {
             const int lh = L * NH + h;
             for (int t = 0; t < nk; ++t, ++it) {
-                const int st = it & (k2::kStages - 1);
+                const int st = it % k2::kStages;
                 if (t == 0) {
                     const int qb = h & 1;
                     ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort));
@@ -570,7 +583,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
                     }
                 }
-                ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it >> 2) & 1) ^ 1, abort));
+                ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it / k2::kStages) & 1) ^ 1, abort));
                 if (!ok) break;
                 const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && blockIdx.x == 0 && blockIdx.y == 0;
                 if (leader && !skip) {
@@ -579,8 +592,6 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
                     tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
                     tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
-                    tma_load_2d(sb + k2::kSBa, &mapB, kv_full + st, k0, h * p.I_pad + xq0);
-                    tma_load_2d(sb + k2::kSBb, &mapB, kv_full + st, k0, h * p.I_pad + xq0 + 128);
                 }
                 __syncwarp();
             }
@@ -616,7 +627,9 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         // addresses < 256 KB)
         const uint64_t dQ0 = sdesc_at(tK, qbase + g * 8192), dK0 = sdesc_at(tK, sbase + k2::kSK);
         const uint64_t dV0 = sdesc_at(tV, sbase + k2::kSV);
-        const uint64_t dB0 = sdesc_at(tV, sbase + (g ? k2::kSBb : k2::kSBa)), dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
+        const uint64_t dB0 = sdesc_at(tV, smem_u32(sm + k2::kBias + g * k2::kBStages * k2::kBiasBytes));
+        const uint64_t dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
+        constexpr uint64_t kBiasStep = k2::kBiasBytes >> 4;
         constexpr uint64_t kStageStep = k2::kStageBytes >> 4;
         bool ok = true;
         // S_g(it) = Q_g K(it)^T + Bias_g(it) I into buffer it & 1: the pair bias is
@@ -626,9 +639,10 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         // colU(g) + 16 h .. + 15 (free until the head's gated output is written there
         // at the start of the next head), and Q K^T reads its A operand from TMEM.
         auto issue_s = [&](int it, int h) {
-            const uint64_t st = static_cast<uint64_t>(it & (k2::kStages - 1));
+            const uint64_t st = static_cast<uint64_t>(it % k2::kStages);
             const uint32_t qt = tmem + k2::colU(g) + h * 16;
-            const uint64_t kb = dK0 + st * kStageStep, bb = dB0 + st * kStageStep;
+            const uint64_t kb = dK0 + st * kStageStep;
+            const uint64_t bb = dB0 + static_cast<uint64_t>(it & (k2::kBStages - 1)) * kBiasStep;
             const uint32_t d = tmem + k2::colS(g, it & 1);
             mma_ts(d, qt, kb, idS, 0u);
             mma_ts(d, qt + 8, kb + 2, idS, 1u);
@@ -637,7 +651,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         };
         // O_g (+)= P_g(it) V'(it); the first tile of a head (t == 0) overwrites
         auto issue_pv = [&](int it, int t) {
-            const uint64_t vb = dV0 + static_cast<uint64_t>(it & (k2::kStages - 1)) * kStageStep;
+            const uint64_t vb = dV0 + static_cast<uint64_t>(it % k2::kStages) * kStageStep;
             const uint32_t a = tmem + k2::colS(g, it & 1), d = tmem + k2::colO(g);
             const uint32_t first = t > 0 ? 1u : 0u;
 #pragma unroll
@@ -647,7 +661,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         auto s_ready = [&](int it, int h, int t) -> bool {
             bool r = true;
             if (t == 0) r = mbar_wait(q_full + (h & 1), (h >> 1) & 1, abort);
-            if (r) r = mbar_wait(kv_full + (it & (k2::kStages - 1)), (it >> 2) & 1, abort);
+            if (r) r = mbar_wait(kv_full + it % k2::kStages, (it / k2::kStages) & 1, abort);
+            if (r) r = mbar_wait(b_full + g * k2::kBStages + (it & (k2::kBStages - 1)), (it >> 2) & 1, abort);
             return __all_sync(0xffffffffu, r);
         };
         auto issue_s_step = [&](int it, int h, int t) {   // leader only
@@ -661,8 +676,15 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
             issue_s(it, h);
             tc_commit(s_full + g * 2 + (it & 1));
+            tc_commit(b_empty + g * k2::kBStages + (it & (k2::kBStages - 1)));   // bias tile read
         };
-        // prologue: S of tiles 0 and 1
+        // prologue: S of tiles 0 and 1.  Group 1 starts about a microsecond later, so
+        // that the two groups' exponential phases and MMA bursts interleave instead of
+        // coinciding; with separate bias rings nothing pulls them back into step.
+        if (g == 1) {
+            __nanosleep(500);
+            __nanosleep(500);
+        }
         int hn = 0, tn = 0;                           // (head, tile) of the next S to issue
         for (int it = 0; ok && it < 2 && it < NT; ++it) {
             ok = s_ready(it, hn, tn);
@@ -686,7 +708,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 tc_fence_after();
                 issue_pv(it, tp);
                 tc_commit(o_ready + g * 2 + (it & 1));
-                tc_commit(kv_empty + (it & (k2::kStages - 1)));   // this group is done with the stage
+                tc_commit(kv_empty + it % k2::kStages);   // this group is done with the K / V' stage
                 if (nx < NT) issue_s_step(nx, hn, tn);
             }
             __syncwarp();
@@ -707,6 +729,40 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             __syncwarp();
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutMma);
+    } else if (warp == 3) {
+        setmaxnreg_dec<120>();
+        // ------------------------------------------------------------ bias producer
+        // Keeps each group's bias ring as full as that group's own progress allows,
+        // polling both rings so a slower group never holds the other's loads back.
+        const bool leader = elect_one();
+        if (leader) prefetch_tmap(&mapB);
+        int nb0 = 0, nb1 = 0;                      // next tile to load, per group
+        bool ok = true;
+        const uint64_t t0 = globaltimer();
+        while (ok && (nb0 < NT || nb1 < NT)) {
+            bool progressed = false;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int j = g ? nb1 : nb0;
+                if (j >= NT) continue;
+                const int bs = g * k2::kBStages + (j & (k2::kBStages - 1));
+                if (!__all_sync(0xffffffffu, mbar_test(b_empty + bs, ((j >> 2) & 1) ^ 1))) continue;
+                if (leader) {
+                    const int h = j / nk, t = j - h * nk;
+                    mbar_arrive_expect_tx(b_full + bs, k2::kBiasBytes);
+                    tma_load_2d(sm + k2::kBias + bs * k2::kBiasBytes, &mapB, b_full + bs, p.k_begin + t * k2::kKT,
+                                h * p.I_pad + xq0 + g * 128);
+                }
+                __syncwarp();
+                if (g) ++nb1; else ++nb0;
+                progressed = true;
+            }
+            if (!progressed) {
+                if (*abort || globaltimer() - t0 > kWaitTimeoutNs) ok = false;
+                else __nanosleep(64);
+            }
+        }
+        if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
     } else if (warp < 4) {
         setmaxnreg_dec<120>();                     // idle warps of the control warpgroup
     } else {
