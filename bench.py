@@ -48,7 +48,7 @@ def parse():
 # operand traffic (q, k, vT, g, bias, out) grows with I^2.  Valid only for the kernel sources it was
 # captured with (hash below); any change to them reports null until the capture is repeated.
 ATTN_TRAFFIC_I512 = 270.8e6 + 48.3e6
-ATTN_TRAFFIC_SRC = "9261bb623f1660c9"
+ATTN_TRAFFIC_SRC = "8fac19596af5db56"
 
 
 def attention_traffic(I: int):

@@ -17,18 +17,20 @@
 //   sm103_ln_proj   persistent; per tile of 128 pair vectors on one line:
 //                   TMA load of Z (128B swizzle), tcgen05 MMA z x [Wq|Wv|Wk|Wg]
 //                   (M=128, N=2x256, K=128) into TMEM, LayerNorm statistics
-//                   and the pair bias on CUDA cores, epilogue writing
-//                   q (scaled by log2(e)/sqrt(d)), k, v^T, sigmoid gate and the
-//                   log2(e)-scaled pair bias (-inf on masked keys) in f16.
+//                   and the pair bias on CUDA cores, four epilogue warpgroups
+//                   writing q (scaled by log2(e)/sqrt(d)), k and the sigmoid
+//                   gate through TMA stores, v^T, and the log2(e)-scaled pair
+//                   bias (a finite -30000 on masked keys), all in f16.
 //   sm103_attention one CTA per (line, 256 queries); two softmax warpgroups
-//                   (128 queries each) ping-pong on the tensor core:
-//                   S = Q K^T (tcgen05, TMEM), online softmax with the bias
-//                   added from the TMA-staged tile, P (f16) written back into
-//                   TMEM over S, O += P V (A operand from TMEM), conditional
-//                   rescaling of O, then normalise, gate, and the output
-//                   projection (u W_o, A operand from TMEM) with the pair
-//                   mask, stored in the node's orientation.  The I x I score
-//                   matrix of a line is never materialised.
+//                   (128 queries each), each with its own MMA-issuing warp:
+//                   S = Q K^T + Bias I (tcgen05 into TMEM; Q copied once per
+//                   head into TMEM, the staged bias tile as an A operand
+//                   against an identity), online softmax with lazy rescaling,
+//                   P (f16) written back into TMEM over S, O += P V (A operand
+//                   from TMEM), then normalise, gate, and the output projection
+//                   (u W_o, A operand from TMEM) with the pair mask, stored in
+//                   the node's orientation.  The I x I score matrix of a line
+//                   is never materialised.
 //
 // Sources: the operation as stated in tri_attn.h (Dell page, Evoformer
 // paragraph; Intel page, steps 2 and 4: bias term and fusing it into the
@@ -597,7 +599,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
         }
         if (ok && p.last) {
-            // W_o^T goes into the Q region once the last S MMAs of both buffers are done
+            // W_o^T goes into the Q region once both MMA issuers have copied the last Q
+            // of each buffer into TMEM
             for (int b = 0; ok && b < 2; ++b) {
                 const int hl = (NH - 1) - (((NH - 1) & 1) != b ? 1 : 0);   // last head h with h & 1 == b
                 ok = __all_sync(0xffffffffu, mbar_wait(q_empty + b, (hl >> 1) & 1, abort));
