@@ -430,7 +430,7 @@ constexpr int kKT = 64;                      // keys per stage (one S sub-tile)
 // freed as soon as that group's S has read it, so the groups do not hold each
 // other's loads back.
 constexpr int kStages = 5;                   // K / V' ring: stage = it % 5, phase = (it / 5) & 1
-constexpr int kBStages = 4;                  // bias ring per group: it & 3, phase (it >> 2) & 1
+constexpr int kBStages = 3;                  // bias ring per group: stage = it % 3, phase = (it / 3) & 1
 constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64)
 constexpr int kStage = 32768;
 constexpr int kSK = 0;                       // K tile: 64 keys x 64 B (SW64)
@@ -440,13 +440,13 @@ constexpr int kStageTx = 4096 + 4096;        // bytes the TMA writes per K / V' 
 constexpr int kBias = kStage + kStages * kStageBytes;    // [2 groups][4] bias tiles: 128 rows x 128 B (SW128)
 constexpr int kBiasBytes = 16384;
 constexpr int kIdent = kBias + 2 * kBStages * kBiasBytes;   // 64 x 64 f16 identity (SW128, K-major)
-constexpr int kBar = kIdent + 8192;
+constexpr int kWo = kIdent + 8192;           // W_o^T, 2 x [128 x 128 B] (SW128), loaded at block start
+constexpr int kBar = kWo + 32768;
 constexpr int kSmem = kBar + 512 + 1024;     // barriers + alignment slack
 // TMEM columns
 __host__ __device__ constexpr uint32_t colS(int g, int b) { return g * 128u + b * 64u; }   // S / P buffers
 __host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 64u; }  // O (32) | row sum l (1)
 __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  // gated u (f16 pairs)
-static_assert(kBStages == 4, "bias stage index and phase are computed with it & 3 and (it >> 2) & 1");
 static_assert(kBias % 1024 == 0 && kIdent % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
 }  // namespace k2
@@ -571,6 +571,12 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             prefetch_tmap(&mapB);
         }
         bool ok = true;
+        if (leader && p.last) {                   // W_o^T for the output projection at the block end
+            prefetch_tmap(&mapWo);
+            mbar_arrive_expect_tx(w_full, 32768);
+            tma_load_2d(sm + k2::kWo, &mapWo, w_full, 0, 0);
+            tma_load_2d(sm + k2::kWo + 16384, &mapWo, w_full, 64, 0);
+        }
         for (int h = 0, it = 0; ok && h < NH; ++h) {
             const int lh = L * NH + h;
             for (int t = 0; t < nk; ++t, ++it) {
@@ -598,19 +604,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 __syncwarp();
             }
         }
-        if (ok && p.last) {
-            // W_o^T goes into the Q region once both MMA issuers have copied the last Q
-            // of each buffer into TMEM
-            for (int b = 0; ok && b < 2; ++b) {
-                const int hl = (NH - 1) - (((NH - 1) & 1) != b ? 1 : 0);   // last head h with h & 1 == b
-                ok = __all_sync(0xffffffffu, mbar_wait(q_empty + b, (hl >> 1) & 1, abort));
-            }
-            if (ok && leader) {
-                prefetch_tmap(&mapWo);
-                mbar_arrive_expect_tx(w_full, 32768);
-                tma_load_2d(sm + k2::kQ, &mapWo, w_full, 0, 0);
-                tma_load_2d(sm + k2::kQ + 16384, &mapWo, w_full, 64, 0);
-            }
+        if (p.last) {
+            // the block must not end with the W_o^T copy still writing its shared
+            // memory, even when another role gave up (bounded, ignores the abort flag)
+            volatile int keep_waiting = 0;
+            mbar_wait(w_full, 0, &keep_waiting);
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
     } else if (warp == 1 || warp == 2) {
@@ -645,7 +643,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const uint64_t st = static_cast<uint64_t>(it % k2::kStages);
             const uint32_t qt = tmem + k2::colU(g) + h * 16;
             const uint64_t kb = dK0 + st * kStageStep;
-            const uint64_t bb = dB0 + static_cast<uint64_t>(it & (k2::kBStages - 1)) * kBiasStep;
+            const uint64_t bb = dB0 + static_cast<uint64_t>(it % k2::kBStages) * kBiasStep;
             const uint32_t d = tmem + k2::colS(g, it & 1);
             mma_ts(d, qt, kb, idS, 0u);
             mma_ts(d, qt + 8, kb + 2, idS, 1u);
@@ -665,7 +663,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             bool r = true;
             if (t == 0) r = mbar_wait(q_full + (h & 1), (h >> 1) & 1, abort);
             if (r) r = mbar_wait(kv_full + it % k2::kStages, (it / k2::kStages) & 1, abort);
-            if (r) r = mbar_wait(b_full + g * k2::kBStages + (it & (k2::kBStages - 1)), (it >> 2) & 1, abort);
+            if (r) r = mbar_wait(b_full + g * k2::kBStages + it % k2::kBStages, (it / k2::kBStages) & 1, abort);
             return __all_sync(0xffffffffu, r);
         };
         auto issue_s_step = [&](int it, int h, int t) {   // leader only
@@ -679,7 +677,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
             issue_s(it, h);
             tc_commit(s_full + g * 2 + (it & 1));
-            tc_commit(b_empty + g * k2::kBStages + (it & (k2::kBStages - 1)));   // bias tile read
+            tc_commit(b_empty + g * k2::kBStages + it % k2::kBStages);   // bias tile read
         };
         // prologue: S of tiles 0 and 1.  Group 1 starts about a microsecond later, so
         // that the two groups' exponential phases and MMA bursts interleave instead of
@@ -726,7 +724,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
-                           sdesc_at(tV, qbase + (kk >> 2) * 16384 + (kk & 3) * 32), idP, kk > 0 ? 1u : 0u);
+                           sdesc_at(tV, smem_u32(sm + k2::kWo) + (kk >> 2) * 16384 + (kk & 3) * 32), idP,
+                           kk > 0 ? 1u : 0u);
                 tc_commit(o_full + g);
             }
             __syncwarp();
@@ -748,8 +747,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             for (int g = 0; g < 2; ++g) {
                 const int j = g ? nb1 : nb0;
                 if (j >= NT) continue;
-                const int bs = g * k2::kBStages + (j & (k2::kBStages - 1));
-                if (!__all_sync(0xffffffffu, mbar_test(b_empty + bs, ((j >> 2) & 1) ^ 1))) continue;
+                const int bs = g * k2::kBStages + j % k2::kBStages;
+                if (!__all_sync(0xffffffffu, mbar_test(b_empty + bs, ((j / k2::kBStages) & 1) ^ 1))) continue;
                 if (leader) {
                     const int h = j / nk, t = j - h * nk;
                     mbar_arrive_expect_tx(b_full + bs, k2::kBiasBytes);
