@@ -43,12 +43,12 @@ def parse():
 
 
 # DRAM traffic of one sm103_attention launch, from one ncu capture of dram__bytes_read.sum +
-# dram__bytes_write.sum at I=512 (start node: 270.8 MB read + 48.3 MB written; summary in
+# dram__bytes_write.sum at I=512 (start node: 270.7 MB read + 48.2 MB written; summary in
 # profiles/dram_traffic_complex_2048_I512.md), scaled to I=2048 by the pair count (x16): the kernel's
 # operand traffic (q, k, vT, g, bias, out) grows with I^2.  Valid only for the kernel sources it was
 # captured with (hash below); any change to them reports null until the capture is repeated.
-ATTN_TRAFFIC_I512 = 270.8e6 + 48.3e6
-ATTN_TRAFFIC_SRC = "8fac19596af5db56"
+ATTN_TRAFFIC_I512 = 270.7e6 + 48.2e6
+ATTN_TRAFFIC_SRC = "866150c63524a8d0"
 
 
 def attention_traffic(I: int):
