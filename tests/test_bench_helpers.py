@@ -1,0 +1,39 @@
+"""Host-side pieces of bench.py: the roofline denominators and the recorded DRAM
+traffic of the attention kernel (reported only while the kernel sources are the
+ones it was captured with)."""
+import json
+import os
+
+import pytest
+
+import bench
+
+
+def test_peaks_are_positive():
+    peak, peak_sus, hbm, src = bench.peaks()
+    assert peak > 0 and hbm > 0 and src in ("measured", "fallback")
+    if src == "measured":
+        with open(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        assert peak == p["bf16_tflops"] and hbm == p["hbm_gbs"]
+
+
+def test_attention_traffic_scales_with_pairs():
+    t512 = bench.attention_traffic(512)
+    if t512 is None:
+        pytest.skip("kernel sources changed since the traffic capture (bench reports null)")
+    assert t512 == pytest.approx(bench.ATTN_TRAFFIC_I512)
+    assert bench.attention_traffic(2048) == pytest.approx(16 * t512)
+
+
+def test_attention_traffic_null_for_other_sources(tmp_path, monkeypatch):
+    # a copy of the kernel sources with one byte changed must not reuse the capture
+    csrc = tmp_path / "protein_pair_representation_gate_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("sm103_kernels.cu", "sm103_ptx.cuh"):
+        src = os.path.join(bench.ROOT, "protein_pair_representation_gate_b300", "csrc", f)
+        with open(src, "rb") as fh:
+            data = fh.read()
+        (csrc / f).write_bytes(data + (b" " if f == "sm103_ptx.cuh" else b""))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.attention_traffic(2048) is None
