@@ -17,6 +17,11 @@ What is computed (the operation the library implements):
     o[i,j,h]= sum_k softmax_k(s_ik) v[k,j,h]
   both:
     out[i,j]= (g[i,j] * concat_h o[i,j,h]) @ W_o + b_o,  and 0 where m[i]*m[j] = 0.
+  optional pair mask M[I, I] (the Evoformer's use; a reading, the pages give no
+  formula): the starting node's row i attends only keys (i, k) with M[i, k] = 1
+  and its output pairs (i, j) with M[i, j] = 0 are 0; the ending node's column j
+  attends keys (k, j) with M[k, j] = 1 and zeroes pairs (i, j) with M[i, j] = 0.
+  optional residual: the result is Z + out (the in-place update Z += out).
 
 Sources on the pages (none prints the formulas; these name the parts):
   * Dell, "PowerEdge XE8545 ... protein model analysis": the Evoformer handles
@@ -152,10 +157,12 @@ def _gate_and_project(o_heads: np.ndarray, g: np.ndarray, w_o, b_o) -> np.ndarra
 
 
 def triangle_attention_starting(Z, mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_gamma, ln_beta, b_g, b_o,
-                                rows=None, key_chunks: int = 1, bias=None) -> np.ndarray:
+                                rows=None, key_chunks: int = 1, bias=None, pair_mask=None) -> np.ndarray:
     """Starting-node triangle attention; returns out[rows, I, c] (all rows by default).
 
     Row i: queries are pairs (i, j), keys/values pairs (i, k), bias b[h, j, k].
+    With a pair mask M, row i's keys and output pairs are further limited to
+    M[i, :] = 1.
     """
     I, _, c = Z.shape
     H = w_b.shape[1]
@@ -168,27 +175,30 @@ def triangle_attention_starting(Z, mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_gamma,
     for r, i in enumerate(rows):
         if not mask[i]:
             continue
+        valid = mask if pair_mask is None else mask & np.asarray(pair_mask[i], dtype=bool)
         zh = layer_norm(Z[i], ln_gamma, ln_beta)                # [I, c]
         q, k, v = _heads(zh @ w_q, H), _heads(zh @ w_k, H), _heads(zh @ w_v, H)
         g = sigmoid(zh @ w_g + b_g)
         o = np.empty_like(q)
         for h in range(H):
             if key_chunks <= 1:
-                o[h] = softmax_attention(q[h], k[h], v[h], bias[h], mask)
+                o[h] = softmax_attention(q[h], k[h], v[h], bias[h], valid)
             else:
-                o[h] = chunked_softmax_attention(q[h], k[h], v[h], bias[h], mask, bounds)
+                o[h] = chunked_softmax_attention(q[h], k[h], v[h], bias[h], valid, bounds)
         out[r] = _gate_and_project(o, g, w_o, b_o)
-        out[r][~mask] = 0.0
+        out[r][~valid] = 0.0
     return out
 
 
 def triangle_attention_ending(Z, mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_gamma, ln_beta, b_g, b_o,
-                              cols=None, key_chunks: int = 1, bias=None) -> np.ndarray:
+                              cols=None, key_chunks: int = 1, bias=None, pair_mask=None) -> np.ndarray:
     """Ending-node triangle attention; returns out[:, cols, c] as [I, len(cols), c].
 
     Column j: queries are pairs (i, j), keys/values pairs (k, j), bias b[h, k, i]
     (the pair bias read transposed).  Written directly, not by transposing Z, so
     that the identity end(Z) = start(Z^T)^T is a check rather than a definition.
+    With a pair mask M, column j's keys and output pairs are further limited to
+    M[:, j] = 1.
     """
     I, _, c = Z.shape
     H = w_b.shape[1]
@@ -201,6 +211,7 @@ def triangle_attention_ending(Z, mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_gamma, l
     for r, j in enumerate(cols):
         if not mask[j]:
             continue
+        valid = mask if pair_mask is None else mask & np.asarray(pair_mask[:, j], dtype=bool)
         zh = layer_norm(Z[:, j], ln_gamma, ln_beta)             # pairs (x, j), x = 0..I-1
         q, k, v = _heads(zh @ w_q, H), _heads(zh @ w_k, H), _heads(zh @ w_v, H)
         g = sigmoid(zh @ w_g + b_g)
@@ -208,24 +219,31 @@ def triangle_attention_ending(Z, mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_gamma, l
         for h in range(H):
             bt = bias[h].T                                      # bt[i, k] = b[h, k, i]
             if key_chunks <= 1:
-                o[h] = softmax_attention(q[h], k[h], v[h], bt, mask)
+                o[h] = softmax_attention(q[h], k[h], v[h], bt, valid)
             else:
-                o[h] = chunked_softmax_attention(q[h], k[h], v[h], bt, mask, bounds)
+                o[h] = chunked_softmax_attention(q[h], k[h], v[h], bt, valid, bounds)
         col = _gate_and_project(o, g, w_o, b_o)                 # [I (i), c]
-        col[~mask] = 0.0
+        col[~valid] = 0.0
         out[:, r] = col
     return out
 
 
-def triangle_attention(node: str, Z, mask, weights: dict, lines=None, key_chunks: int = 1, bias=None):
+def triangle_attention(node: str, Z, mask, weights: dict, lines=None, key_chunks: int = 1, bias=None,
+                       pair_mask=None, residual: bool = False):
     """Dispatch by node.  `lines` selects output rows (start) or columns (end).
 
     Returns out for the selected lines in the orientation of Z:
-    start -> [len(lines), I, c]; end -> [I, len(lines), c].
+    start -> [len(lines), I, c]; end -> [I, len(lines), c].  With residual=True
+    it returns Z + out over the same pairs.
     """
     w = {k: weights[k] for k in ("w_q", "w_k", "w_v", "w_g", "w_b", "w_o", "ln_gamma", "ln_beta", "b_g", "b_o")}
+    sel = range(Z.shape[0]) if lines is None else list(lines)
     if node == "start":
-        return triangle_attention_starting(Z, mask, rows=lines, key_chunks=key_chunks, bias=bias, **w)
+        out = triangle_attention_starting(Z, mask, rows=lines, key_chunks=key_chunks, bias=bias,
+                                          pair_mask=pair_mask, **w)
+        return Z[sel] + out if residual else out
     if node == "end":
-        return triangle_attention_ending(Z, mask, cols=lines, key_chunks=key_chunks, bias=bias, **w)
+        out = triangle_attention_ending(Z, mask, cols=lines, key_chunks=key_chunks, bias=bias,
+                                        pair_mask=pair_mask, **w)
+        return Z[:, sel] + out if residual else out
     raise ValueError(f"node must be 'start' or 'end', got {node!r}")

@@ -41,7 +41,7 @@ def _gate_after_projection(o_heads, g, w_o, b_o):
 
 
 def _swapped_roles_ending(Z, mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_gamma, ln_beta, b_g, b_o,
-                          cols=None, key_chunks=1, bias=None):
+                          cols=None, key_chunks=1, bias=None, pair_mask=None):
     # keys/values taken along the row instead of down the column
     out = T.triangle_attention_starting(Z.transpose(1, 0, 2).copy(), mask, w_q, w_k, w_v, w_g, w_b, w_o,
                                         ln_gamma, ln_beta, b_g, b_o, key_chunks=key_chunks)

@@ -298,3 +298,105 @@ def test_brute_force_scalar_loops():
                         u.append(g * sum(w[t] * vals[t][e] for t in range(len(w))) / tot)
                 want = [sum(u[x] * p["w_o"][x][n] for x in range(H * d)) + p["b_o"][n] for n in range(c)]
                 np.testing.assert_allclose(out[i, j], want, atol=1e-12)
+
+
+# ---------------------------------------------------------------- pair mask and residual
+
+def _pair_mask(I, seed, p_valid=0.7):
+    rng = np.random.default_rng(seed)
+    return rng.random((I, I)) < p_valid
+
+
+def test_pair_mask_brute_force_scalar_loops():
+    """Catches a pair mask applied to the wrong pair (transposed, or the query's
+    instead of the key's): scalar loops on a 4-token problem, both nodes."""
+    import math
+    I, c, H, d = 4, 4, 2, 2
+    p = small_problem(I=I, c=c, H=H, d=d, seed=43, n_pad=0)
+    p["mask"][3] = False
+    M = _pair_mask(I, 5)
+    M[0, 1] = True
+    Z, m = p["Z"], p["mask"]
+
+    def ln(x):
+        mu = sum(x) / len(x)
+        var = sum((t - mu) ** 2 for t in x) / len(x)
+        return [(t - mu) / math.sqrt(var + 1e-5) * p["ln_gamma"][a] + p["ln_beta"][a] for a, t in enumerate(x)]
+
+    def lin(x, w, col):
+        return sum(x[a] * w[a][col] for a in range(len(x)))
+
+    zh = [[ln(list(Z[a, b])) for b in range(I)] for a in range(I)]
+    for node in ("start", "end"):
+        out = O.triangle_attention(node, Z, m, weights(p), pair_mask=M)
+        for i in range(I):
+            for j in range(I):
+                if not (m[i] and m[j] and M[i, j]):
+                    assert all(out[i, j] == 0.0)
+                    continue
+                u = []
+                for h in range(H):
+                    qv = [lin(zh[i][j], p["w_q"], h * d + e) for e in range(d)]
+                    scores, vals = [], []
+                    for k in range(I):
+                        kp, bp = ((i, k), (j, k)) if node == "start" else ((k, j), (k, i))
+                        if not (m[k] and M[kp[0], kp[1]]):
+                            continue
+                        kv = [lin(zh[kp[0]][kp[1]], p["w_k"], h * d + e) for e in range(d)]
+                        s = sum(qv[e] * kv[e] for e in range(d)) / math.sqrt(d) + lin(zh[bp[0]][bp[1]], p["w_b"], h)
+                        scores.append(s)
+                        vals.append([lin(zh[kp[0]][kp[1]], p["w_v"], h * d + e) for e in range(d)])
+                    mx = max(scores)
+                    w = [math.exp(s - mx) for s in scores]
+                    tot = sum(w)
+                    for e in range(d):
+                        g = 1.0 / (1.0 + math.exp(-(lin(zh[i][j], p["w_g"], h * d + e) + p["b_g"][h * d + e])))
+                        u.append(g * sum(w[t] * vals[t][e] for t in range(len(w))) / tot)
+                want = [sum(u[x] * p["w_o"][x][n] for x in range(H * d)) + p["b_o"][n] for n in range(c)]
+                np.testing.assert_allclose(out[i, j], want, atol=1e-12)
+
+
+def test_pair_mask_of_token_mask_equals_token_mask():
+    """Catches a pair mask that changes anything beyond the token mask it encodes."""
+    p = small_problem(I=9, n_pad=2, seed=17)
+    M = np.outer(p["mask"], p["mask"])
+    for node in ("start", "end"):
+        np.testing.assert_allclose(O.triangle_attention(node, p["Z"], p["mask"], weights(p), pair_mask=M),
+                                   run(node, p), atol=1e-13)
+
+
+@pytest.mark.parametrize("node", ["start", "end"])
+def test_masked_key_pair_has_no_influence_on_its_line(node):
+    """Catches a masked key still entering the softmax: perturbing Z at a pair that
+    is masked as a key leaves that line's outputs unchanged."""
+    p = small_problem(I=8, seed=19)
+    M = _pair_mask(8, 7, 0.8)
+    line, key = 2, 5
+    if node == "start":
+        M[line, key] = False
+    else:
+        M[key, line] = False
+    base = O.triangle_attention(node, p["Z"], p["mask"], weights(p), pair_mask=M)
+    q = dict(p)
+    q["Z"] = p["Z"].copy()
+    if node == "start":
+        q["Z"][line, key] += 3.0 * rand(23, 0, p["Z"].shape[-1])
+    else:
+        q["Z"][key, line] += 3.0 * rand(23, 0, p["Z"].shape[-1])
+    pert = O.triangle_attention(node, q["Z"], q["mask"], weights(q), pair_mask=M)
+    if node == "start":
+        np.testing.assert_allclose(pert[line], base[line], atol=1e-12)
+        assert not np.allclose(pert, base)               # the pair still feeds other lines' bias
+    else:
+        np.testing.assert_allclose(pert[:, line], base[:, line], atol=1e-12)
+        assert not np.allclose(pert, base)
+
+
+def test_residual_with_everything_masked_returns_z():
+    """Catches a residual that scales or drops Z: with every pair masked the
+    update is exactly 0, so the result is Z itself."""
+    p = small_problem(I=6, seed=29)
+    M = np.zeros((6, 6), dtype=bool)
+    for node in ("start", "end"):
+        got = O.triangle_attention(node, p["Z"], p["mask"], weights(p), pair_mask=M, residual=True)
+        np.testing.assert_array_equal(got, p["Z"])
