@@ -143,6 +143,31 @@ tri_attn_status tri_attn_forward(tri_attn_ctx* ctx, int node, int I,
                                  void* workspace, size_t workspace_bytes,
                                  void* out, void* stream);
 
+/* Options of tri_attn_forward_ex (a host struct; NULL means all defaults).
+ *   pair_mask  [I, I] uint8 device array over the pairs (i, j) of Z, row-major,
+ *              nonzero = valid pair, or NULL (all valid).  Starting node: line i
+ *              attends only keys (i, k) with pair_mask[i, k] != 0; ending node:
+ *              line j attends only keys (k, j) with pair_mask[k, j] != 0; in both
+ *              the output of a pair with pair_mask[i, j] == 0 is 0.  It acts on
+ *              top of token_mask.  (The sources name masking but print no formula;
+ *              this follows the token-mask reading pair by pair.)
+ *   residual   nonzero: write Z + update (rounded once to the dtype) instead of the
+ *              update; out may then be Z itself (in-place update Z += update). */
+typedef struct {
+    const uint8_t* pair_mask;
+    int residual;
+} tri_attn_options;
+
+/* tri_attn_forward with options.  Arguments as for tri_attn_forward, except that
+ * with opt->residual set `out` may equal Z (a partial overlap is still EINVAL).
+ * tri_attn_forward(...) is tri_attn_forward_ex(..., opt = NULL, ...). */
+tri_attn_status tri_attn_forward_ex(tri_attn_ctx* ctx, int node, int I,
+                                    const void* Z, const uint8_t* token_mask,
+                                    const tri_attn_options* opt,
+                                    const tri_attn_weights* w,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* out, void* stream);
+
 /* Synchronise `stream`, then read and clear the context's device status word.
  * Returns ETIMEOUT if a kernel gave up a bounded wait since the last call,
  * ECUDA if the stream reports an error, else OK. */

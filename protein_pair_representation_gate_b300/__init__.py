@@ -36,13 +36,16 @@ class TriangleAttention:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         return self._ws
 
-    def __call__(self, node, Z, weights: dict, mask=None, out=None, stream=None):
+    def __call__(self, node, Z, weights: dict, mask=None, out=None, stream=None, pair_mask=None,
+                 residual: bool = False):
+        """out = update (or Z + update with residual=True; pass out=Z for the in-place Z += update).
+        pair_mask: optional [I, I] uint8 device tensor over the pairs of Z."""
         import torch
         I = Z.shape[0]
         if out is None:
             out = torch.empty_like(Z)
         ws = self.workspace(I, Z.device)
-        self.ctx.forward(node, I, Z, mask, weights, ws, out, stream)
+        self.ctx.forward(node, I, Z, mask, weights, ws, out, stream, pair_mask=pair_mask, residual=residual)
         return out
 
 

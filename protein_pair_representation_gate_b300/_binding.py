@@ -21,7 +21,7 @@ NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
 
 EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
            "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
-           "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject")
+           "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject", "tri_attn_forward_ex")
 FAULT_NONE, FAULT_SKIP_STAGE = 0, 1
 
 
@@ -40,6 +40,10 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("ln_gamma", "ln_beta", "w_q", "w_k", "w_v", "w_g", "w_b", "b_g", "w_o", "b_o")]
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("pair_mask", ctypes.c_void_p), ("residual", ctypes.c_int)]
 
 
 _lib = None
@@ -65,6 +69,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tri_attn_workspace_bytes.restype = sz
     lib.tri_attn_forward.argtypes = [vp, i, i, vp, vp, ctypes.POINTER(Weights), vp, sz, vp, vp]
     lib.tri_attn_forward.restype = i
+    lib.tri_attn_forward_ex.argtypes = [vp, i, i, vp, vp, ctypes.POINTER(Options), ctypes.POINTER(Weights), vp, sz,
+                                        vp, vp]
+    lib.tri_attn_forward_ex.restype = i
     lib.tri_attn_status_sync.argtypes = [vp, vp]
     lib.tri_attn_status_sync.restype = i
     lib.tri_attn_set_timing.argtypes = [vp, i]
@@ -161,19 +168,27 @@ class TriAttn:
         return int(self.lib.tri_attn_workspace_bytes(self._h, I))
 
     def forward(self, node, I: int, Z, mask, weights: dict, workspace, out, stream=None,
-                workspace_bytes: int | None = None) -> int:
-        """tri_attn_forward on device tensors (or raw pointers); raises on a non-OK status."""
-        st = self.forward_status(node, I, Z, mask, weights, workspace, out, stream, workspace_bytes)
+                workspace_bytes: int | None = None, pair_mask=None, residual: bool = False) -> int:
+        """tri_attn_forward(_ex) on device tensors (or raw pointers); raises on a non-OK status."""
+        st = self.forward_status(node, I, Z, mask, weights, workspace, out, stream, workspace_bytes,
+                                 pair_mask=pair_mask, residual=residual)
         if st != OK:
             raise TriAttnError(st, "tri_attn_forward")
         return st
 
-    def forward_status(self, node, I, Z, mask, weights, workspace, out, stream=None, workspace_bytes=None) -> int:
+    def forward_status(self, node, I, Z, mask, weights, workspace, out, stream=None, workspace_bytes=None,
+                       pair_mask=None, residual: bool = False) -> int:
+        """tri_attn_forward, or tri_attn_forward_ex when a pair mask or the residual is asked for."""
         w = Weights(*[_ptr(weights.get(n)) for n, _ in Weights._fields_])
         if workspace_bytes is None:
             workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
-        return self.lib.tri_attn_forward(self._h, NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(w),
-                                         _ptr(workspace), workspace_bytes, _ptr(out), _stream_ptr(stream))
+        if pair_mask is None and not residual:
+            return self.lib.tri_attn_forward(self._h, NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(w),
+                                             _ptr(workspace), workspace_bytes, _ptr(out), _stream_ptr(stream))
+        opt = Options(_ptr(pair_mask), 1 if residual else 0)
+        return self.lib.tri_attn_forward_ex(self._h, NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(opt),
+                                            ctypes.byref(w), _ptr(workspace), workspace_bytes, _ptr(out),
+                                            _stream_ptr(stream))
 
     def status_sync(self, stream=None) -> int:
         return self.lib.tri_attn_status_sync(self._h, _stream_ptr(stream))

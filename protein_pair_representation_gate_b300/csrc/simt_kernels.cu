@@ -115,6 +115,8 @@ struct AttnArgs {
     int I, I_pad, H, d, C;
     int k_begin, k_end, first, last;
     const uint8_t* mask;
+    const uint8_t* pmask;      // [I, I] pair mask over the pairs of Z, or NULL
+    int node;
     const float *q, *k, *v, *g, *bias;
     float *u, *o_run, *lse_run;
 };
@@ -156,7 +158,10 @@ __global__ void __launch_bounds__(128) simt_attention(AttnArgs a) {
 #pragma unroll
         for (int yy = 0; yy < kKeyTile; ++yy) {
             float t = -INFINITY;
-            if (yy < nk) {
+            const int key = y0 + yy;
+            const bool key_ok = a.pmask == nullptr ||
+                                a.pmask[a.node == TRI_ATTN_STARTING ? (size_t)L * a.I + key : (size_t)key * a.I + L] != 0;
+            if (yy < nk && key_ok) {
                 t = brow[y0 + yy];
 #pragma unroll
                 for (int e = 0; e < D; ++e) t = fmaf(q[e], ks[yy][e], t);
@@ -213,9 +218,11 @@ __global__ void __launch_bounds__(128) simt_attention(AttnArgs a) {
 struct OutArgs {
     int node, I, I_pad, c, C;
     const uint8_t* mask;
+    const uint8_t* pmask;      // [I, I] pair mask, or NULL
     const float* u;
     const void* w_o;
     const float* b_o;
+    const void* Z;             // residual source (NULL: write the update only)
     void* out;
 };
 
@@ -245,9 +252,12 @@ __global__ void __launch_bounds__(128) simt_out_proj(OutArgs a) {
         for (int p = 0; p < kPairs; ++p) {
             const int x = x0 + p;
             if (x >= a.I) break;
-            const bool ok = line_ok && (a.mask == nullptr || a.mask[x] != 0);
             const size_t pair = a.node == TRI_ATTN_STARTING ? (size_t)L * a.I + x : (size_t)x * a.I + L;
-            out[pair * a.c + n] = stf<T>(ok ? acc[p] + bo : 0.f);
+            const bool ok = line_ok && (a.mask == nullptr || a.mask[x] != 0) &&
+                            (a.pmask == nullptr || a.pmask[pair] != 0);
+            float v = ok ? acc[p] + bo : 0.f;
+            if (a.Z) v += ldf(static_cast<const T*>(a.Z), pair * a.c + n);   // in place: read before write
+            out[pair * a.c + n] = stf<T>(v);
         }
     }
 }
@@ -279,7 +289,7 @@ cudaError_t simt_forward_t(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     const int cs = chunk_size(a.I, a.key_chunks);
     for (int k0 = 0; k0 < a.I; k0 += cs) {
         const int k1 = k0 + cs < a.I ? k0 + cs : a.I;
-        AttnArgs aa{a.I, a.I_pad, a.H, a.d, C, k0, k1, k0 == 0, k1 == a.I, a.mask,
+        AttnArgs aa{a.I, a.I_pad, a.H, a.d, C, k0, k1, k0 == 0, k1 == a.I, a.mask, a.pair_mask, a.node,
                     f(W.q), f(W.k), f(W.v), f(W.g), f(W.bias), f(W.u),
                     W.o_run ? f(W.o_run) : nullptr, W.lse_run ? f(W.lse_run) : nullptr};
         if (tm) tm->begin("simt_attention", s);
@@ -294,7 +304,8 @@ cudaError_t simt_forward_t(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         if (tm) tm->end(s);
         if (e != cudaSuccess) return e;
     }
-    OutArgs oa{a.node, a.I, a.I_pad, a.c_z, C, a.mask, f(W.u), a.w.w_o, a.w.b_o, a.out};
+    OutArgs oa{a.node, a.I, a.I_pad, a.c_z, C, a.mask, a.pair_mask, f(W.u), a.w.w_o, a.w.b_o,
+               a.residual ? a.Z : nullptr, a.out};
     {
         dim3 grid((a.I + kPairs - 1) / kPairs, a.I);
         if (tm) tm->begin("simt_out_proj", s);

@@ -415,12 +415,34 @@ struct AttnParams {
     int node, I, I_pad, nk, k_begin, k_end, first, last;
     int inject;                // test hook: block (0,0) skips the load of stage 1
     const uint8_t* mask;
+    const uint8_t* pmask;      // [I, I] pair mask over the pairs of Z, or NULL
+    const uint64_t* kbits;     // [I][I_pad / 64 + 1] key-valid bits per line (with pmask), or NULL
     const __half* g;
     const float* bo;
     float *o_run, *lse_run;
+    const __nv_bfloat16* Z;    // residual source (NULL: write the update only); may equal out
     __nv_bfloat16* out;
     uint32_t* status;
 };
+
+// Key-valid bits of each line under a pair mask: bit kk of word w of line L is
+// set when key w*64 + kk < I and the pair mask admits it on that line (starting
+// node: M[L, key]; ending node: M[key, L]).  One extra zero word per line lets a
+// key tile that starts off a 64-key boundary (key chunks) read two words.
+__global__ void __launch_bounds__(128) sm103_pair_keybits(const uint8_t* pm, int node, int I, int words,
+                                                          uint64_t* kbits) {
+    const int idx = blockIdx.x * 128 + threadIdx.x;
+    if (idx >= I * words) return;
+    const int L = idx / words, w = idx % words;
+    uint64_t bits = 0;
+    for (int kk = 0; kk < 64; ++kk) {
+        const int key = w * 64 + kk;
+        if (key >= I) break;
+        const uint8_t v = node == TRI_ATTN_STARTING ? pm[(size_t)L * I + key] : pm[(size_t)key * I + L];
+        if (v) bits |= 1ull << kk;
+    }
+    kbits[idx] = bits;
+}
 
 namespace k2 {
 constexpr int kThreads = 384;                // control warpgroup (producer, 2 MMA issuers, 1 idle) + 2 softmax warpgroups
@@ -434,49 +456,68 @@ constexpr int kBStages = 3;                  // bias ring per group: stage = it 
 constexpr int kQ = 0;                        // [2 bufs][2 tiles][128 x 64 B] (SW64)
 constexpr int kStage = 32768;
 constexpr int kSK = 0;                       // K tile: 64 keys x 64 B (SW64)
-constexpr int kSV = 4096;                    // V' tile: 32 rows V^T + 16 rows [1; 0], 128 B each (SW128)
+constexpr int kSV = 4096;                    // V' tile: 32 rows V^T + 16 more rows (below), 128 B each (SW128)
+constexpr int kSM = kSV + 4096;              // rows 32..39 of V': M, the pair-mask row (64 keys x 16 B, no swizzle)
 constexpr int kStageBytes = 10240;
 constexpr int kStageTx = 4096 + 4096;        // bytes the TMA writes per K / V' stage
 constexpr int kBias = kStage + kStages * kStageBytes;    // [2 groups][4] bias tiles: 128 rows x 128 B (SW128)
 constexpr int kBiasBytes = 16384;
-constexpr int kIdent = kBias + 2 * kBStages * kBiasBytes;   // 64 x 64 f16 identity (SW128, K-major)
-constexpr int kWo = kIdent + 8192;           // W_o^T, 2 x [128 x 128 B] (SW128), loaded at block start
-constexpr int kBar = kWo + 32768;
-constexpr int kSmem = kBar + 512 + 1024;     // barriers + alignment slack
+// The kernel comes in two builds: the plain forward (kEx = false) and the one
+// with a pair mask and / or a residual (kEx = true), so that the plain forward
+// carries none of their code.  With a pair mask, one more K-step adds E M^T to S,
+// E (128 x 16) holding 1.0 in column 0 and the stage's M (64 x 16) 0 or -30000 in
+// column 0 (the key is admitted or excluded on this line).  Both without swizzle;
+// columns 8..15 of E are a block of zeros, those of M the stage's ones and zero
+// rows (finite).  The ones row of V' then moves from row 32 to row 40.
+template <bool kEx>
+struct Lay {
+    static constexpr int kME = kBias + 2 * kBStages * kBiasBytes;   // E: 128 rows x 16 B, then 2 KB of zeros
+    static constexpr int kIdent = kME + (kEx ? 4096 : 0);            // 64 x 64 f16 identity (SW128, K-major)
+    static constexpr int kWo = kIdent + 8192;     // W_o^T, 2 x [128 x 128 B] (SW128), loaded at block start
+    static constexpr int kBar = kWo + 32768;
+    static constexpr int kSmem = kBar + 512 + 1024;   // barriers + alignment slack
+    static constexpr int kLCol = kEx ? 40 : 32;   // row of V' holding ones = column of P V' holding l
+    static_assert(kIdent % 1024 == 0 && kWo % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+    static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
+};
 // TMEM columns
 __host__ __device__ constexpr uint32_t colS(int g, int b) { return g * 128u + b * 64u; }   // S / P buffers
-__host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 64u; }  // O (32) | row sum l (1)
+__host__ __device__ constexpr uint32_t colO(int g) { return 256u + g * 64u; }  // O (32), row sum l (kLCol)
 __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  // gated u (f16 pairs)
-static_assert(kBias % 1024 == 0 && kIdent % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
-static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
+static_assert(kBias % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 }  // namespace k2
 
+template <bool kEx>
 __global__ void __launch_bounds__(k2::kThreads, 1)
 sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapWo, AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
+    using LY = k2::Lay<kEx>;
     if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     const int L = blockIdx.y;
     const int xq0 = blockIdx.x * 256;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (p.mask != nullptr && p.mask[L] == 0) {
-        // the whole line is padding: its outputs are zero
-        if (p.last) {
+        // the whole line is padding: its update is zero (with a residual: out = Z)
+        if (p.last && (!kEx || p.Z != p.out)) {
             const size_t sL = p.node == TRI_ATTN_STARTING ? (size_t)p.I * CZ : CZ;
             const size_t sX = p.node == TRI_ATTN_STARTING ? CZ : (size_t)p.I * CZ;
             for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
                 const int x = xq0 + i / 16;
-                if (x < p.I)
-                    reinterpret_cast<uint4*>(p.out + L * sL + x * sX)[i % 16] = make_uint4(0, 0, 0, 0);
+                if (x < p.I) {
+                    const size_t at = L * sL + x * sX;
+                    reinterpret_cast<uint4*>(p.out + at)[i % 16] =
+                        (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z + at)[i % 16] : make_uint4(0, 0, 0, 0);
+                }
             }
         }
         return;
     }
 
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + k2::kBar);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::kBar);
     uint64_t* q_full = bars + 0;      // [2]
     uint64_t* q_empty = bars + 2;     // [2]
     uint64_t* kv_full = bars + 48;    // [5]
@@ -495,12 +536,15 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     uint64_t* b_full = bars + 32;     // [2 groups][4]: bias tile staged
     uint64_t* b_empty = bars + 40;    // [2 groups][4]: S of that tile done (bias read)
 
-    // Rows 32..47 of each stage's V': a row of ones (gives the softmax row sum as
-    // output column 32 of P V') and 15 zero rows.  Same in every swizzle phase.
+    // Rows 32..47 of each stage's V': a row of ones (row kLCol: gives the softmax
+    // row sum as output column kLCol of P V'), the rest zero.  With kEx, rows
+    // 32..39 hold the pair-mask tile M (zero without a pair mask; as rows of V'
+    // they only fill columns 32..39 of P V', which nothing reads).  Same in every
+    // swizzle phase.
     for (int i = threadIdx.x; i < k2::kStages * 2048 / 16; i += blockDim.x) {
         const int st = i / 128, off = (i % 128) * 16;
-        uint8_t* dst = sm + k2::kStage + st * k2::kStageBytes + k2::kSV + 4096 + off;
-        const uint32_t one2 = off < 128 ? 0x3C003C00u : 0u;
+        uint8_t* dst = sm + k2::kStage + st * k2::kStageBytes + k2::kSM + off;
+        const uint32_t one2 = (off >= (LY::kLCol - 32) * 128 && off < (LY::kLCol - 31) * 128) ? 0x3C003C00u : 0u;
         *reinterpret_cast<uint4*>(dst) = make_uint4(one2, one2, one2, one2);
     }
     // 64 x 64 identity, the B operand that adds the staged bias tile into S:
@@ -513,8 +557,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const int e = n & 7;                              // column n within the chunk
             w[e >> 1] = (e & 1) ? 0x3C000000u : 0x00003C00u;
         }
-        *reinterpret_cast<uint4*>(sm + k2::kIdent + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sm + LY::kIdent + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    if (kEx && p.kbits != nullptr)             // E: 1.0 in column 0, then its columns 8..15: zeros
+        for (int i = threadIdx.x; i < 4096 / 16; i += blockDim.x)
+            *reinterpret_cast<uint4*>(sm + LY::kME + i * 16) = make_uint4(i < 128 ? 0x3C00u : 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
 
     const int nk = p.nk;
@@ -574,8 +621,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         if (leader && p.last) {                   // W_o^T for the output projection at the block end
             prefetch_tmap(&mapWo);
             mbar_arrive_expect_tx(w_full, 32768);
-            tma_load_2d(sm + k2::kWo, &mapWo, w_full, 0, 0);
-            tma_load_2d(sm + k2::kWo + 16384, &mapWo, w_full, 64, 0);
+            tma_load_2d(sm + LY::kWo, &mapWo, w_full, 0, 0);
+            tma_load_2d(sm + LY::kWo + 16384, &mapWo, w_full, 64, 0);
         }
         for (int h = 0, it = 0; ok && h < NH; ++h) {
             const int lh = L * NH + h;
@@ -591,8 +638,24 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
                     }
                 }
+                uint32_t two = 0;                 // key-valid bits of keys k0 + 2 lane, + 1 (read before the wait;
+                if (kEx && p.kbits != nullptr) {  // k0 is a multiple of 8, so both bits sit in one 32-bit word)
+                    // (lane and line re-read here: keeping the block-start values live into this
+                    // branch costs the kernel-wide register allocation a spill)
+                    const int k = p.k_begin + t * k2::kKT + 2 * static_cast<int>(lane_id());
+                    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(p.kbits + (size_t)blockIdx.y * (p.I_pad / 64 + 1));
+                    two = wrow[k >> 5] >> (k & 31);
+                }
                 ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it / k2::kStages) & 1) ^ 1, abort));
                 if (!ok) break;
+                if (kEx && p.kbits != nullptr) {  // M of the stage: lane writes keys 2 lane, 2 lane + 1
+                    const uint32_t ln = lane_id();
+                    uint8_t* mt = sm + k2::kStage + st * k2::kStageBytes + k2::kSM + (ln >> 2) * 128 + (ln & 3) * 32;
+                    *reinterpret_cast<uint16_t*>(mt) = (two & 1u) ? uint16_t(0) : uint16_t(0xF753u);   // f16 -30000
+                    *reinterpret_cast<uint16_t*>(mt + 16) = (two & 2u) ? uint16_t(0) : uint16_t(0xF753u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && blockIdx.x == 0 && blockIdx.y == 0;
                 if (leader && !skip) {
                     const int k0 = p.k_begin + t * k2::kKT;
@@ -629,9 +692,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const uint64_t dQ0 = sdesc_at(tK, qbase + g * 8192), dK0 = sdesc_at(tK, sbase + k2::kSK);
         const uint64_t dV0 = sdesc_at(tV, sbase + k2::kSV);
         const uint64_t dB0 = sdesc_at(tV, smem_u32(sm + k2::kBias + g * k2::kBStages * k2::kBiasBytes));
-        const uint64_t dI = sdesc_at(tV, smem_u32(sm + k2::kIdent));
+        const uint64_t dI = sdesc_at(tV, smem_u32(sm + LY::kIdent));
         constexpr uint64_t kBiasStep = k2::kBiasBytes >> 4;
         constexpr uint64_t kStageStep = k2::kStageBytes >> 4;
+        const uint64_t dE = sdesc_noswizzle(smem_u32(sm + LY::kME), 2048, 128);
+        const uint64_t dM0 = sdesc_noswizzle(sbase + k2::kSM, 1024, 128);
         bool ok = true;
         // S_g(it) = Q_g K(it)^T + Bias_g(it) I into buffer it & 1: the pair bias is
         // added by the tensor core (the staged bias tile is the A operand of four
@@ -649,6 +714,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mma_ts(d, qt + 8, kb + 2, idS, 1u);
 #pragma unroll
             for (int kk = 0; kk < k2::kKT / 16; ++kk) mma_ss(d, bb + kk * 2, dI + kk * 2, idS, 1u);
+            if (kEx && p.kbits != nullptr) mma_ss(d, dE, dM0 + st * kStageStep, idS, 1u);   // -30000 on excluded keys
         };
         // O_g (+)= P_g(it) V'(it); the first tile of a head (t == 0) overwrites
         auto issue_pv = [&](int it, int t) {
@@ -724,7 +790,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
-                           sdesc_at(tV, smem_u32(sm + k2::kWo) + (kk >> 2) * 16384 + (kk & 3) * 32), idP,
+                           sdesc_at(tV, smem_u32(sm + LY::kWo) + (kk >> 2) * 16384 + (kk & 3) * 32), idP,
                            kk > 0 ? 1u : 0u);
                 tc_commit(o_full + g);
             }
@@ -791,7 +857,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         auto finalize = [&](int hp) {
             uint32_t ov[32];
             tmem_ld32(tO, ov);
-            const float l = __uint_as_float(tmem_ld1(tO + 32));
+            const float l = __uint_as_float(tmem_ld1(tO + LY::kLCol));
             tmem_ld_wait();
             float o[HD];
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -866,6 +932,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 for (int k = 0; k < k2::kKT; ++k)
                     if (k >= nvalid) s[k] = -INFINITY;
             }
+
             // P V'(it-2) is long complete: observing it every tile keeps the o_ready
             // phases in step for the waits on P V'(it-1) below.  The test is issued
             // here and its result used only at the end of the tile.
@@ -910,7 +977,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     if (!wait_prev_pv()) { ok = false; break; }
                     uint32_t ov[32];
                     tmem_ld32(tO, ov);
-                    uint32_t lv = tmem_ld1(tO + 32);
+                    uint32_t lv = tmem_ld1(tO + LY::kLCol);
                     tmem_ld_wait();
                     const float mn = need ? mt : m;
                     const float alpha = ex2(m - mn);
@@ -918,7 +985,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
                     lv = __float_as_uint(__uint_as_float(lv) * alpha);
                     tmem_st32(tO, ov);
-                    tmem_st1(tO + 32, lv);
+                    tmem_st1(tO + LY::kLCol, lv);
                     m = mn;
                 }
                 const float negm = -m;
@@ -948,20 +1015,37 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (lane == 0) mbar_arrive(u_full + g);
             if (mbar_wait(o_full + g, 0, abort)) {
                 tc_fence_after();
-                const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
                 const size_t pair = p.node == TRI_ATTN_STARTING ? (size_t)L * p.I + x : (size_t)x * p.I + L;
+                const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0) &&
+                                   (!kEx || p.pmask == nullptr || p.pmask[pair] != 0);
                 uint4* dst = reinterpret_cast<uint4*>(p.out + pair * CZ);
+                const uint4* zres = (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z + pair * CZ) : nullptr;
                 const uint32_t tOut = tl + k2::colS(g, 0);
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t v[32];
                     tmem_ld32(tOut + cb * 32, v);
                     tmem_ld_wait();
+                    uint32_t zw[16];                     // residual (this thread's own pair: read before write)
+                    if constexpr (kEx) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4 zv = (zres && x < p.I) ? zres[cb * 4 + i] : make_uint4(0, 0, 0, 0);
+                            zw[4 * i] = zv.x;
+                            zw[4 * i + 1] = zv.y;
+                            zw[4 * i + 2] = zv.z;
+                            zw[4 * i + 3] = zv.w;
+                        }
+                    }
                     uint32_t o[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float a0 = valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f;
-                        const float a1 = valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f;
+                        float a0 = valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f;
+                        float a1 = valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f;
+                        if constexpr (kEx) {
+                            a0 += bf16lo(zw[e >> 1]);
+                            a1 += bf16hi(zw[e >> 1]);
+                        }
                         o[e >> 1] = pack_bf16(a0, a1);
                     }
                     if (x < p.I) {
@@ -1054,7 +1138,11 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(sm103_ln_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::kSmem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sm103_attention, cudaFuncAttributeMaxDynamicSharedMemorySize, k2::kSmem);
+        e = cudaFuncSetAttribute(sm103_attention<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 k2::Lay<false>::kSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(sm103_attention<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 k2::Lay<true>::kSmem);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
@@ -1119,6 +1207,16 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         !map2d(&mB, hf(W.bias), Ip, (uint64_t)NH * Ip, (uint64_t)Ip * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !map2d(&mWo, hf(W.wo_t), CH, CZ, CH * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    uint64_t* kbits = nullptr;
+    if (a.pair_mask != nullptr) {
+        kbits = reinterpret_cast<uint64_t*>(a.ws + W.kbits);
+        const int words = Ip / 64 + 1;
+        if (tm) tm->begin("sm103_pair_keybits", s);
+        sm103_pair_keybits<<<(I * words + 127) / 128, 128, 0, s>>>(a.pair_mask, a.node, I, words, kbits);
+        if (tm) tm->end(s);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int cs = chunk_size(I, a.key_chunks);
     for (int k0 = 0; k0 < I; k0 += cs) {
         const int k1e = k0 + cs < I ? k0 + cs : I;
@@ -1132,6 +1230,9 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.first = k0 == 0;
         ap.last = k1e == I;
         ap.mask = a.mask;
+        ap.pmask = a.pair_mask;
+        ap.kbits = kbits;
+        ap.Z = a.residual ? static_cast<const __nv_bfloat16*>(a.Z) : nullptr;
         ap.g = hf(W.g);
         ap.bo = f32(W.bo);
         ap.o_run = W.o_run ? f32(W.o_run) : nullptr;
@@ -1141,7 +1242,10 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.inject = k0 == 0 ? a.inject : 0;
         dim3 grid(Ip / 256, I);
         if (tm) tm->begin("sm103_attention", s);
-        sm103_attention<<<grid, k2::kThreads, k2::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+        if (ap.kbits != nullptr || ap.Z != nullptr)
+            sm103_attention<true><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+        else
+            sm103_attention<false><<<grid, k2::kThreads, k2::Lay<false>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

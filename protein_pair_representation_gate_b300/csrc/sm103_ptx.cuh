@@ -183,6 +183,20 @@ __host__ __device__ __forceinline__ constexpr uint64_t sdesc_tmpl(uint32_t sbo, 
     return (static_cast<uint64_t>(1u) << 16) | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
            (static_cast<uint64_t>(1u) << 46) | (static_cast<uint64_t>(swizzle) << 61);
 }
+// Descriptor of a K-major operand without swizzle: 8-row x 16-byte core
+// matrices, the two K-adjacent core matrices of one K = 16 step `lbo` bytes
+// apart, 8-row groups `sbo` bytes apart.
+// The lane index read from its special register each time (volatile: not merged
+// with an earlier read, so no block-start value has to stay live).
+__device__ __forceinline__ uint32_t lane_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1u) << 46);
+}
 // descriptor template + start address (16-byte units)
 __device__ __forceinline__ uint64_t sdesc_at(uint64_t tmpl, uint32_t saddr) {
     return tmpl | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);

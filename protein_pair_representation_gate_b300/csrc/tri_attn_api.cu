@@ -138,6 +138,12 @@ size_t tri_attn_workspace_bytes(const tri_attn_ctx* c, int I) {
 tri_attn_status tri_attn_forward(tri_attn_ctx* c, int node, int I, const void* Z, const uint8_t* mask,
                                  const tri_attn_weights* w, void* workspace, size_t workspace_bytes,
                                  void* out, void* stream) {
+    return tri_attn_forward_ex(c, node, I, Z, mask, nullptr, w, workspace, workspace_bytes, out, stream);
+}
+
+tri_attn_status tri_attn_forward_ex(tri_attn_ctx* c, int node, int I, const void* Z, const uint8_t* mask,
+                                    const tri_attn_options* opt, const tri_attn_weights* w, void* workspace,
+                                    size_t workspace_bytes, void* out, void* stream) {
     if (!c || !Z || !w || !workspace || !out) return TRI_ATTN_EINVAL;
     const tri_attn_config& g = c->cfg;
     if (node != TRI_ATTN_STARTING && node != TRI_ATTN_ENDING) return TRI_ATTN_EINVAL;
@@ -152,7 +158,12 @@ tri_attn_status tri_attn_forward(tri_attn_ctx* c, int node, int I, const void* Z
     if (workspace_bytes < lay.total) return TRI_ATTN_ENOMEM;
     const size_t esz = g.dtype == TRI_ATTN_F32 ? 4 : 2;
     const size_t pair_bytes = (size_t)I * I * g.c_z * esz;
-    if (overlaps(out, pair_bytes, Z, pair_bytes) || overlaps(out, pair_bytes, workspace, lay.total))
+    const bool residual = opt && opt->residual;
+    const bool in_place = residual && out == Z;          // the one overlap allowed: Z += update
+    if ((!in_place && overlaps(out, pair_bytes, Z, pair_bytes)) || overlaps(out, pair_bytes, workspace, lay.total))
+        return TRI_ATTN_EINVAL;
+    const uint8_t* pmask = opt ? opt->pair_mask : nullptr;
+    if (pmask && (overlaps(pmask, (size_t)I * I, out, pair_bytes) || overlaps(pmask, (size_t)I * I, workspace, lay.total)))
         return TRI_ATTN_EINVAL;
 
     FwdArgs a;
@@ -172,6 +183,8 @@ tri_attn_status tri_attn_forward(tri_attn_ctx* c, int node, int I, const void* Z
     a.key_chunks = g.key_chunks;
     a.status = c->d_status;
     a.inject = c->inject;
+    a.pair_mask = pmask;
+    a.residual = residual ? 1 : 0;
     c->inject = 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -40,6 +40,7 @@ struct Workspace {
     size_t o_run = 0, lse_run = 0;                          // key-chunk state (0 bytes if unchunked)
     size_t wprep = 0, colsum = 0, betaw = 0, wb32 = 0, wo_t = 0, bo = 0;  // prepared weights (sm103)
     size_t cst = 0;                                          // per column pair {colsum x2, offset x2} (sm103)
+    size_t kbits = 0;                                        // [I][I_pad / 64 + 1] key-valid bits per line (sm103)
     size_t total = 0;
 };
 
@@ -58,6 +59,8 @@ struct FwdArgs {
     int key_chunks;
     uint32_t* status;        // device status word
     int inject = 0;          // test hook (tri_attn_debug_inject)
+    const uint8_t* pair_mask = nullptr;   // [I, I] over the pairs of Z, or NULL
+    int residual = 0;        // write Z + update
 };
 
 // Records an event pair around a launch when timing is on.
@@ -90,6 +93,7 @@ constexpr Workspace sm103_layout(int I, int key_chunks) {
     w.wo_t = take((size_t)128 * 128 * 2);    // W_o^T, f16
     w.bo = take(128 * 4);
     w.cst = take(256 * 4 * 4);
+    w.kbits = take((size_t)I * (w.I_pad / 64 + 1) * 8);
     w.q = take(P * 128 * 2);
     w.k = take(P * 128 * 2);
     w.v = take(P * 128 * 2);

@@ -113,3 +113,21 @@ def test_debug_inject_arguments():
     tc = B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "bf16"))
     assert tc.debug_inject(7) == B.EINVAL
     assert tc.debug_inject(B.FAULT_NONE) == B.OK
+
+
+def test_forward_ex_aliasing_rules(setup):
+    """out may equal Z only with the residual; a partial overlap is always EINVAL;
+    validation errors launch nothing."""
+    torch, t, ctx, ws = setup
+    Z = t["Z"].clone()
+    before = Z.clone()
+    nb = ws.numel()
+    assert ctx.forward_status(0, 64, Z, t["mask"], t, ws, Z, None, nb) == B.EINVAL
+    pm = torch.ones(64, 64, dtype=torch.uint8, device="cuda")
+    assert ctx.forward_status(0, 64, Z, t["mask"], t, ws, Z, None, nb, residual=False, pair_mask=pm) == B.EINVAL
+    shifted = Z.data_ptr() + 16 * 128
+    assert ctx.forward_status(0, 64, Z, t["mask"], t, ws, shifted, None, nb, residual=True) == B.EINVAL
+    torch.cuda.synchronize()
+    assert torch.equal(Z, before)
+    assert ctx.forward_status(0, 64, Z, t["mask"], t, ws, Z, None, nb, residual=True) == B.OK
+    assert ctx.status_sync() == B.OK
