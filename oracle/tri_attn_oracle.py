@@ -23,6 +23,15 @@ What is computed (the operation the library implements):
   attends keys (k, j) with M[k, j] = 1 and zeroes pairs (i, j) with M[i, j] = 0.
   optional residual: the result is Z + out (the in-place update Z += out).
 
+  MSA row-wise gated self-attention with pair bias (the same attention with
+  another batch and bias source): for an MSA representation Ms[S, I, c_m], a
+  pair representation Z[I, I, c_z] and a mask mm[S, I],
+    mh      = LayerNorm_m(Ms);  q, k, v, g from mh as above
+    b[h]    = LayerNorm_z(Z) @ W_b[:, h]          (shared by all S rows)
+  row s, head h, query i, keys j with mm[s, j] = 1:
+    o[s,i,h]= sum_j softmax_j(q[s,i,h] . k[s,j,h] / sqrt(d) + b[h, i, j]) v[s,j,h]
+    out[s,i]= (g[s,i] * concat_h o[s,i,h]) @ W_o + b_o, and 0 where mm[s, i] = 0.
+
 Sources on the pages (none prints the formulas; these name the parts):
   * Dell, "PowerEdge XE8545 ... protein model analysis": the Evoformer handles
     the residue-pair graph with triangle self-attention (Evoformer paragraph).
@@ -30,6 +39,9 @@ Sources on the pages (none prints the formulas; these name the parts):
     and step 4: self-attention learns triangle-geometry constraints over the
     pair representation; the attention module carries a large bias term
     computed by tensor contractions from the pair tensor.
+  * Intel, step 4 (the attention-slicing example): the attention call takes
+    the query rows, a per-row (batched) mask bias and one bias shared by all
+    rows (non-batched, from the pair representation) -- the MSA row form.
   * OpenFold-TRT summary (gist.science), Methodology: bf16 Evoformer core.
   * Design-CP summary (gist.science), Methodology 1: keys/values processed in
     pieces with scores formed on the fly (ring attention), self-attention
@@ -247,3 +259,38 @@ def triangle_attention(node: str, Z, mask, weights: dict, lines=None, key_chunks
                                         pair_mask=pair_mask, **w)
         return Z[:, sel] + out if residual else out
     raise ValueError(f"node must be 'start' or 'end', got {node!r}")
+
+
+def msa_row_attention(Ms, Z, msa_mask, w_q, w_k, w_v, w_g, w_b, w_o, ln_m_gamma, ln_m_beta, ln_z_gamma,
+                      ln_z_beta, b_g, b_o, rows=None, bias=None, residual: bool = False) -> np.ndarray:
+    """MSA row-wise gated self-attention with pair bias; returns [len(rows), I, c_m].
+
+    Row s of the MSA representation Ms[S, I, c_m] attends over its own residues:
+    queries (s, i), keys/values (s, j) with msa_mask[s, j] = 1, and the per-head
+    bias b[h, i, j] = LayerNorm_z(Z[i, j]) @ W_b[:, h] from the pair
+    representation, the same for every row (the non-batched bias of the Intel
+    page's attention call, step 4; the per-row mask is its batched bias).  The
+    MSA and the pair tensor have LayerNorms of their own.  Outputs at masked
+    positions (s, i) are 0; with residual=True the result is Ms + out.
+    """
+    S, I, _ = Ms.shape
+    H = w_b.shape[1]
+    msa_mask = np.asarray(msa_mask, dtype=bool)
+    rows = range(S) if rows is None else rows
+    if bias is None:
+        bias = pair_bias(Z, ln_z_gamma, ln_z_beta, w_b)         # [H, I (query i), I (key j)]
+    out = np.zeros((len(rows), I, w_o.shape[1]), dtype=np.float64)
+    for r, s in enumerate(rows):
+        valid = msa_mask[s]
+        if valid.any():
+            mh = layer_norm(Ms[s], ln_m_gamma, ln_m_beta)       # [I, c_m]
+            q, k, v = _heads(mh @ w_q, H), _heads(mh @ w_k, H), _heads(mh @ w_v, H)
+            g = sigmoid(mh @ w_g + b_g)
+            o = np.empty_like(q)
+            for h in range(H):
+                o[h] = softmax_attention(q[h], k[h], v[h], bias[h], valid)
+            out[r] = _gate_and_project(o, g, w_o, b_o)
+            out[r][~valid] = 0.0
+    if residual:
+        out = np.asarray(Ms, dtype=np.float64)[list(rows)] + out
+    return out
