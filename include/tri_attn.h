@@ -168,6 +168,67 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* ctx, int node, int I,
                                     void* workspace, size_t workspace_bytes,
                                     void* out, void* stream);
 
+/* MSA row-wise gated self-attention with pair bias: the same attention with
+ * another batch and bias source.  For an MSA representation Ms[S, I, c_m], a
+ * pair representation Z[I, I, c_z] and a mask mm[S, I]:
+ *
+ *   mh      = LayerNorm_m(Ms);  q, k, v = mh W_q, mh W_k, mh W_v;  g = sigmoid(mh W_g + b_g)
+ *   b[h]    = LayerNorm_z(Z) W_b[:, h]                   shared by all S rows
+ *   row s, head h, query (s, i), keys (s, j) with mm[s, j] != 0:
+ *     o[s,i,h] = sum_j softmax_j( q[s,i,h].k[s,j,h] / sqrt(d) + b[h,i,j] ) v[s,j,h]
+ *   out[s,i] = (g[s,i] * concat_h o[s,i,h]) W_o + b_o,  0 where mm[s, i] == 0
+ *              (with residual: Ms + that, rounded once to the dtype).
+ *
+ * Source: "通量提升达 23.11 倍！至强可扩展平台助力 AlphaFold2 端到端优化" (Intel),
+ * step 4: the Evoformer's attention call takes the query rows, a per-row
+ * (batched) mask bias and a bias shared by all rows (non-batched, from the pair
+ * representation).  Readings: the MSA and Z have LayerNorms of their own (the
+ * context's ln_eps for both); the MSA mask excludes keys and zeroes outputs as
+ * the pair mask of tri_attn_forward_ex does.
+ *
+ * The context supplies c_z (pair channels), heads, head_dim, dtype, ln_eps and
+ * key_chunks; it runs on the CUDA-core kernels (any context path; head_dim 8,
+ * 16, 32 or 64), fp32 arithmetic on dtype storage. */
+typedef struct {
+    const float* ln_m_gamma;  /* [c_m] fp32                   */
+    const float* ln_m_beta;   /* [c_m] fp32                   */
+    const void*  w_q;         /* [c_m, C] dtype               */
+    const void*  w_k;         /* [c_m, C] dtype               */
+    const void*  w_v;         /* [c_m, C] dtype               */
+    const void*  w_g;         /* [c_m, C] dtype               */
+    const float* b_g;         /* [C] fp32                     */
+    const void*  w_o;         /* [C, c_m] dtype               */
+    const float* b_o;         /* [c_m] fp32, or NULL for zero */
+    const float* ln_z_gamma;  /* [c_z] fp32                   */
+    const float* ln_z_beta;   /* [c_z] fp32                   */
+    const void*  w_b;         /* [c_z, H] dtype               */
+} tri_attn_msa_weights;
+
+/* Bytes of device workspace tri_attn_msa_forward needs for S rows of I
+ * residues (0 for a NULL context, S outside 1..16384 or I outside 1..I_max).
+ * Same ownership rules as tri_attn_workspace_bytes. */
+size_t tri_attn_msa_workspace_bytes(const tri_attn_ctx* ctx, int S, int I);
+
+/*   S           MSA rows, 1 <= S <= 16384
+ *   I           residues, 1 <= I <= cfg.I_max
+ *   c_m         MSA channels, 1 <= c_m <= 256
+ *   msa         Ms [S, I, c_m] dtype, row-major, 16-byte aligned
+ *   msa_mask    [S, I] uint8 (nonzero = valid), or NULL for all valid
+ *   Z           [I, I, cfg.c_z] dtype, row-major, 16-byte aligned
+ *   w           parameters (struct itself is host memory; device pointers)
+ *   residual    nonzero: write Ms + update; out may then be msa itself
+ *   workspace   >= tri_attn_msa_workspace_bytes(ctx, S, I) bytes, 256-byte aligned
+ *   out         [S, I, c_m] dtype, 16-byte aligned; must not overlap Z, the
+ *               workspace or msa_mask, nor msa unless it is msa itself with residual
+ *               (msa_mask must not lie in the workspace either)
+ * Asynchronous; EINVAL / EUNSUPPORTED / ENOMEM from validation without
+ * launching, ECUDA if a launch fails. */
+tri_attn_status tri_attn_msa_forward(tri_attn_ctx* ctx, int S, int I, int c_m,
+                                     const void* msa, const uint8_t* msa_mask, const void* Z,
+                                     const tri_attn_msa_weights* w, int residual,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* out, void* stream);
+
 /* Synchronise `stream`, then read and clear the context's device status word.
  * Returns ETIMEOUT if a kernel gave up a bounded wait since the last call,
  * ECUDA if the stream reports an error, else OK. */

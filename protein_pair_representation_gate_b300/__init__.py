@@ -1,4 +1,5 @@
-"""B300-native gated triangle self-attention (starting and ending node).
+"""B300-native gated triangle self-attention (starting and ending node), and
+MSA row attention with pair bias.
 
 The computation runs in libtriattn.so (hand-written CUDA for sm_103a, C ABI in
 include/tri_attn.h); this package is its Python binding.  torch provides
@@ -49,5 +50,41 @@ class TriangleAttention:
         return out
 
 
-__all__ = ["TriangleAttention", "TriAttn", "TriAttnConfig", "TriAttnError", "load_library", "status_string",
+MSA_WEIGHT_NAMES = ("ln_m_gamma", "ln_m_beta", "w_q", "w_k", "w_v", "w_g", "b_g", "w_o", "b_o",
+                    "ln_z_gamma", "ln_z_beta", "w_b")
+
+
+class MSARowAttention:
+    """MSA row-wise gated attention with pair bias: out = op(msa, Z, weights).
+
+    msa [S, I, c_m] and Z [I, I, c_z] are torch CUDA tensors (tri_attn.h,
+    tri_attn_msa_forward); weights holds MSA_WEIGHT_NAMES; msa_mask is an
+    optional [S, I] uint8 tensor.  Returns `out` ([S, I, c_m]).
+    """
+
+    def __init__(self, c_z: int, heads: int, head_dim: int, I_max: int, dtype: str = "bf16",
+                 key_chunks: int = 1, ln_eps: float = 1e-5):
+        self.ctx = TriAttn(TriAttnConfig(c_z, heads, head_dim, I_max, dtype, ln_eps, key_chunks, True))
+        self._ws = None
+
+    def workspace(self, S: int, I: int, device):
+        import torch
+        need = self.ctx.msa_workspace_bytes(S, I)
+        if self._ws is None or self._ws.numel() < need or self._ws.device != device:
+            self._ws = None
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        return self._ws
+
+    def __call__(self, msa, Z, weights: dict, msa_mask=None, out=None, residual: bool = False, stream=None):
+        """out = update (or msa + update with residual=True; out=msa updates in place)."""
+        import torch
+        S, I, c_m = msa.shape
+        if out is None:
+            out = torch.empty_like(msa)
+        ws = self.workspace(S, I, msa.device)
+        self.ctx.msa_forward(S, I, c_m, msa, msa_mask, Z, weights, ws, out, residual=residual, stream=stream)
+        return out
+
+
+__all__ = ["TriangleAttention", "MSARowAttention", "MSA_WEIGHT_NAMES", "TriAttn", "TriAttnConfig", "TriAttnError", "load_library", "status_string",
            "STARTING", "ENDING", "F32", "BF16", "PATH_SIMT", "PATH_SM103", "EXPORTS", "WEIGHT_NAMES"]

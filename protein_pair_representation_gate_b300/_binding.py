@@ -21,7 +21,8 @@ NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
 
 EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
            "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
-           "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject", "tri_attn_forward_ex")
+           "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject", "tri_attn_forward_ex",
+           "tri_attn_msa_workspace_bytes", "tri_attn_msa_forward")
 FAULT_NONE, FAULT_SKIP_STAGE = 0, 1
 
 
@@ -44,6 +45,12 @@ class Weights(ctypes.Structure):
 
 class Options(ctypes.Structure):
     _fields_ = [("pair_mask", ctypes.c_void_p), ("residual", ctypes.c_int)]
+
+
+class MsaWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("ln_m_gamma", "ln_m_beta", "w_q", "w_k", "w_v", "w_g", "b_g", "w_o", "b_o",
+                 "ln_z_gamma", "ln_z_beta", "w_b")]
 
 
 _lib = None
@@ -72,6 +79,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tri_attn_forward_ex.argtypes = [vp, i, i, vp, vp, ctypes.POINTER(Options), ctypes.POINTER(Weights), vp, sz,
                                         vp, vp]
     lib.tri_attn_forward_ex.restype = i
+    lib.tri_attn_msa_workspace_bytes.argtypes = [vp, i, i]
+    lib.tri_attn_msa_workspace_bytes.restype = sz
+    lib.tri_attn_msa_forward.argtypes = [vp, i, i, i, vp, vp, vp, ctypes.POINTER(MsaWeights), i, vp, sz, vp, vp]
+    lib.tri_attn_msa_forward.restype = i
     lib.tri_attn_status_sync.argtypes = [vp, vp]
     lib.tri_attn_status_sync.restype = i
     lib.tri_attn_set_timing.argtypes = [vp, i]
@@ -189,6 +200,25 @@ class TriAttn:
         return self.lib.tri_attn_forward_ex(self._h, NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(opt),
                                             ctypes.byref(w), _ptr(workspace), workspace_bytes, _ptr(out),
                                             _stream_ptr(stream))
+
+    def msa_workspace_bytes(self, S: int, I: int) -> int:
+        return int(self.lib.tri_attn_msa_workspace_bytes(self._h, S, I))
+
+    def msa_forward_status(self, S: int, I: int, c_m: int, msa, msa_mask, Z, weights: dict, workspace, out,
+                           residual: bool = False, stream=None, workspace_bytes: int | None = None) -> int:
+        """tri_attn_msa_forward on device tensors (or raw pointers); returns the status."""
+        w = MsaWeights(*[_ptr(weights.get(n)) for n, _ in MsaWeights._fields_])
+        if workspace_bytes is None:
+            workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+        return self.lib.tri_attn_msa_forward(self._h, S, I, c_m, _ptr(msa), _ptr(msa_mask), _ptr(Z), ctypes.byref(w),
+                                             1 if residual else 0, _ptr(workspace), workspace_bytes, _ptr(out),
+                                             _stream_ptr(stream))
+
+    def msa_forward(self, *args, **kw) -> int:
+        st = self.msa_forward_status(*args, **kw)
+        if st != OK:
+            raise TriAttnError(st, "tri_attn_msa_forward")
+        return st
 
     def status_sync(self, stream=None) -> int:
         return self.lib.tri_attn_status_sync(self._h, _stream_ptr(stream))

@@ -1,4 +1,6 @@
-// SIMT (CUDA-core, fp32 arithmetic) path of the gated triangle attention.
+// SIMT (CUDA-core, fp32 arithmetic) path of the gated triangle attention, and
+// of MSA row attention with pair bias (the same kernels over S rows of an MSA
+// tensor, the bias projected from the pair tensor in a pass of its own).
 //
 // Three kernels per forward (per key chunk for the attention one):
 //   simt_ln_proj    LayerNorm + q/k/v/gate/pair-bias projections, line-major
@@ -76,9 +78,12 @@ __global__ void __launch_bounds__(256) simt_ln_proj(ProjArgs a) {
     }
     __syncthreads();
 
-    // Projections: thread owns output column `col` for all 16 pairs.
-    const int ncols = 4 * C + a.H;
-    for (int col = threadIdx.x; col < ncols; col += blockDim.x) {
+    // Projections: thread owns output column `col` for all 16 pairs.  Columns
+    // 0 .. 4C-1 are q | k | v | g, the last H the pair bias; a NULL q skips the
+    // former and a NULL bias the latter (the two passes of MSA row attention).
+    const int col0 = a.q != nullptr ? 0 : 4 * C;
+    const int ncols = a.bias != nullptr ? 4 * C + a.H : 4 * C;
+    for (int col = col0 + threadIdx.x; col < ncols; col += blockDim.x) {
         const int which = col < 4 * C ? col / C : 4;
         const int cw = which < 4 ? col - which * C : col - 4 * C;
         const T* W = static_cast<const T*>(which == 0 ? a.w_q : which == 1 ? a.w_k : which == 2 ? a.w_v
@@ -315,7 +320,92 @@ cudaError_t simt_forward_t(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t simt_msa_forward_t(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm) {
+    const Workspace& W = *a.lay;
+    const int C = a.H * a.d;
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(a.ws + off); };
+    cudaError_t e;
+    // pair bias b[h, i, j] = LN_z(Z[i, j]) W_b[:, h]: lines i of Z, bias columns only
+    ProjArgs pz{TRI_ATTN_STARTING, a.I, a.I_pad, a.c_z, a.H, a.d, a.eps, 0.f, a.Z, nullptr,
+                a.w.ln_z_gamma, a.w.ln_z_beta, nullptr, nullptr, nullptr, nullptr, nullptr, a.w.w_b,
+                nullptr, nullptr, nullptr, nullptr, f(W.bias)};
+    {
+        dim3 grid(a.I_pad / kPairs, a.I);
+        if (tm) tm->begin("simt_ln_proj", s);
+        simt_ln_proj<T><<<grid, 256, kPairs * a.c_z * sizeof(float), s>>>(pz);
+        if (tm) tm->end(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // q, k, v, g of the MSA rows: lines s of Ms (row-major [S, I, c_m], the
+    // starting orientation), no bias columns
+    ProjArgs pm{TRI_ATTN_STARTING, a.I, a.I_pad, a.c_m, a.H, a.d, a.eps, kLog2e / sqrtf((float)a.d), a.M, nullptr,
+                a.w.ln_m_gamma, a.w.ln_m_beta, a.w.b_g, a.w.w_q, a.w.w_k, a.w.w_v, a.w.w_g, nullptr,
+                f(W.q), f(W.k), f(W.v), f(W.g), nullptr};
+    {
+        dim3 grid(a.I_pad / kPairs, a.S);
+        if (tm) tm->begin("simt_ln_proj", s);
+        simt_ln_proj<T><<<grid, 256, kPairs * a.c_m * sizeof(float), s>>>(pm);
+        if (tm) tm->end(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // row s attends over its residues; the MSA mask acts as a pair mask over [S, I]
+    const int cs = chunk_size(a.I, a.key_chunks);
+    for (int k0 = 0; k0 < a.I; k0 += cs) {
+        const int k1 = k0 + cs < a.I ? k0 + cs : a.I;
+        AttnArgs aa{a.I, a.I_pad, a.H, a.d, C, k0, k1, k0 == 0, k1 == a.I, nullptr, a.msa_mask, TRI_ATTN_STARTING,
+                    f(W.q), f(W.k), f(W.v), f(W.g), f(W.bias), f(W.u),
+                    W.o_run ? f(W.o_run) : nullptr, W.lse_run ? f(W.lse_run) : nullptr};
+        if (tm) tm->begin("simt_attention", s);
+        switch (a.d) {
+            case 8: e = launch_attention<8>(aa, a.I_pad, a.H, a.S, s); break;
+            case 16: e = launch_attention<16>(aa, a.I_pad, a.H, a.S, s); break;
+            case 32: e = launch_attention<32>(aa, a.I_pad, a.H, a.S, s); break;
+            case 64: e = launch_attention<64>(aa, a.I_pad, a.H, a.S, s); break;
+            default: e = cudaErrorInvalidValue;
+        }
+        if (tm) tm->end(s);
+        if (e != cudaSuccess) return e;
+    }
+    OutArgs oa{TRI_ATTN_STARTING, a.I, a.I_pad, a.c_m, C, nullptr, a.msa_mask, f(W.u), a.w.w_o, a.w.b_o,
+               a.residual ? a.M : nullptr, a.out};
+    {
+        dim3 grid((a.I + kPairs - 1) / kPairs, a.S);
+        if (tm) tm->begin("simt_out_proj", s);
+        simt_out_proj<T><<<grid, 128, kPairs * C * sizeof(float), s>>>(oa);
+        if (tm) tm->end(s);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+Workspace simt_msa_layout(int S, int I, int H, int d, int key_chunks) {
+    Workspace w;
+    w.I = I;
+    w.I_pad = round_up(I, kTile);
+    const size_t P = (size_t)S * w.I_pad;          // row-major (MSA row, residue) slots
+    const size_t C = (size_t)H * d;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    w.q = take(P * C * 4);
+    w.k = take(P * C * 4);
+    w.v = take(P * C * 4);
+    w.g = take(P * C * 4);
+    w.u = take(P * C * 4);
+    w.bias = take((size_t)H * w.I_pad * w.I_pad * 4);
+    if (key_chunks > 1) {
+        w.o_run = take(P * C * 4);
+        w.lse_run = take(P * H * 4);
+    }
+    w.total = off;
+    return w;
+}
+
+cudaError_t simt_msa_forward(const MsaArgs& a, int dtype, cudaStream_t s, LaunchTimer* t) {
+    if (a.d != 8 && a.d != 16 && a.d != 32 && a.d != 64) return cudaErrorInvalidValue;
+    return dtype == TRI_ATTN_F32 ? simt_msa_forward_t<float>(a, s, t) : simt_msa_forward_t<__nv_bfloat16>(a, s, t);
+}
 
 Workspace simt_layout(int I, int c_z, int H, int d, int key_chunks) {
     (void)c_z;

@@ -197,6 +197,66 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* c, int node, int I, const void
     return TRI_ATTN_OK;
 }
 
+size_t tri_attn_msa_workspace_bytes(const tri_attn_ctx* c, int S, int I) {
+    if (!c || S < 1 || S > kMsaMaxRows || I < 1 || I > c->cfg.I_max) return 0;
+    return simt_msa_layout(S, I, c->cfg.heads, c->cfg.head_dim, c->cfg.key_chunks).total;
+}
+
+tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, const void* msa, const uint8_t* msa_mask,
+                                     const void* Z, const tri_attn_msa_weights* w, int residual, void* workspace,
+                                     size_t workspace_bytes, void* out, void* stream) {
+    if (!c || !msa || !Z || !w || !workspace || !out) return TRI_ATTN_EINVAL;
+    const tri_attn_config& g = c->cfg;
+    if (S < 1 || S > kMsaMaxRows || I < 1 || I > g.I_max || c_m < 1 || c_m > 256) return TRI_ATTN_EINVAL;
+    if (g.head_dim != 8 && g.head_dim != 16 && g.head_dim != 32 && g.head_dim != 64) return TRI_ATTN_EUNSUPPORTED;
+    if (!w->ln_m_gamma || !w->ln_m_beta || !w->w_q || !w->w_k || !w->w_v || !w->w_g || !w->b_g || !w->w_o ||
+        !w->ln_z_gamma || !w->ln_z_beta || !w->w_b)
+        return TRI_ATTN_EINVAL;
+    if (!aligned(msa, 16) || !aligned(Z, 16) || !aligned(out, 16) || !aligned(workspace, 256)) return TRI_ATTN_EINVAL;
+    const void* wp[] = {w->ln_m_gamma, w->ln_m_beta, w->w_q, w->w_k, w->w_v, w->w_g, w->b_g, w->w_o, w->b_o,
+                        w->ln_z_gamma, w->ln_z_beta, w->w_b};
+    for (const void* p : wp)
+        if (p && !aligned(p, 16)) return TRI_ATTN_EINVAL;
+    const Workspace lay = simt_msa_layout(S, I, g.heads, g.head_dim, g.key_chunks);
+    if (workspace_bytes < lay.total) return TRI_ATTN_ENOMEM;
+    const size_t esz = g.dtype == TRI_ATTN_F32 ? 4 : 2;
+    const size_t msa_bytes = (size_t)S * I * c_m * esz, z_bytes = (size_t)I * I * g.c_z * esz;
+    const bool in_place = residual && out == msa;        // the one overlap allowed: Ms += update
+    if ((!in_place && overlaps(out, msa_bytes, msa, msa_bytes)) || overlaps(out, msa_bytes, Z, z_bytes) ||
+        overlaps(out, msa_bytes, workspace, lay.total))
+        return TRI_ATTN_EINVAL;
+    if (msa_mask && (overlaps(msa_mask, (size_t)S * I, out, msa_bytes) ||
+                     overlaps(msa_mask, (size_t)S * I, workspace, lay.total)))
+        return TRI_ATTN_EINVAL;
+
+    MsaArgs a;
+    a.S = S;
+    a.I = I;
+    a.I_pad = lay.I_pad;
+    a.c_m = c_m;
+    a.c_z = g.c_z;
+    a.H = g.heads;
+    a.d = g.head_dim;
+    a.key_chunks = g.key_chunks;
+    a.residual = residual ? 1 : 0;
+    a.eps = g.ln_eps;
+    a.M = msa;
+    a.msa_mask = msa_mask;
+    a.Z = Z;
+    a.w = *w;
+    a.ws = static_cast<char*>(workspace);
+    a.lay = &lay;
+    a.out = out;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LaunchTimer* t = c->timing ? &c->timer : nullptr;
+    const cudaError_t e = simt_msa_forward(a, g.dtype, s, t);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "tri_attn_msa_forward: %s\n", cudaGetErrorString(e));
+        return TRI_ATTN_ECUDA;
+    }
+    return TRI_ATTN_OK;
+}
+
 tri_attn_status tri_attn_status_sync(tri_attn_ctx* c, void* stream) {
     if (!c) return TRI_ATTN_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

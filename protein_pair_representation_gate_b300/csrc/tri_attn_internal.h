@@ -74,6 +74,22 @@ struct LaunchTimer {
 Workspace simt_layout(int I, int c_z, int H, int d, int key_chunks);
 cudaError_t simt_forward(const FwdArgs& a, int dtype, cudaStream_t s, LaunchTimer* t);
 
+// MSA row attention with pair bias (CUDA-core kernels).
+struct MsaArgs {
+    int S, I, I_pad, c_m, c_z, H, d, key_chunks, residual;
+    float eps;
+    const void* M;                 // [S, I, c_m]
+    const uint8_t* msa_mask;       // [S, I] or NULL
+    const void* Z;                 // [I, I, c_z]
+    tri_attn_msa_weights w;
+    char* ws;
+    const Workspace* lay;
+    void* out;                     // [S, I, c_m]
+};
+constexpr int kMsaMaxRows = 16384;
+Workspace simt_msa_layout(int S, int I, int H, int d, int key_chunks);
+cudaError_t simt_msa_forward(const MsaArgs& a, int dtype, cudaStream_t s, LaunchTimer* t);
+
 // sm103 path (bf16, c_z = 128, H = 4, d = 32).
 bool sm103_supported(int c_z, int H, int d, int dtype);
 

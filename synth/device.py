@@ -29,3 +29,8 @@ def inputs_to_device(inp: Inputs, device="cuda", pin: bool = False) -> dict:
         else:
             out[n] = t.to(device)
     return out
+
+
+def msa_inputs_to_device(inp, device="cuda") -> dict:
+    """MSA inputs as tensors keyed like tri_attn_msa_weights, plus "Ms", "Z" and "msa_mask"."""
+    return {n: to_torch(getattr(inp, n)).to(device) for n in inp.TENSORS + ("msa_mask",)}

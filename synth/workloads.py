@@ -206,3 +206,119 @@ def make_inputs(wl: Workload | str, I: int | None = None) -> Inputs:
         b_g=np.ones(C, dtype=np.float32),
         b_o=np.zeros(c, dtype=np.float32),
     )
+
+
+# ---------------------------------------------------------------- MSA row attention
+# Inputs of MSA row-wise attention with pair bias: an MSA representation
+# Ms[S, I, c_m] ~ N(0, 1) (stream 10), a pair representation Z[I, I, c_z] ~ N(0, 1)
+# (stream 11), the MSA-side projections ~ N(0, 1/c_m) (streams 1, 2, 3, 5), the
+# pair-bias projection ~ N(0, 1/c_z) (stream 4), W_o ~ N(0, 1/(H d)) (stream 6);
+# LayerNorm gamma = 1, beta = 0 on both sides, gate bias 1, output bias 0.  The
+# MSA mask: the last `pad_rows` rows are padding (all 0), the last `n_pad`
+# residues are padding in every row, and every other position is a gap (0)
+# with probability `p_gap` (uniforms of stream 12).
+STREAM_MSA, STREAM_MSA_Z, STREAM_MSA_MASK = 10, 11, 12
+
+
+@dataclass(frozen=True)
+class MsaWorkload:
+    name: str
+    S: int                     # MSA rows
+    I: int                     # residues
+    c_m: int
+    c_z: int
+    heads: int
+    head_dim: int
+    dtype: str
+    n_pad: int = 0
+    pad_rows: int = 0
+    p_gap: float = 0.0
+    seed: int = 0
+
+    @property
+    def C(self) -> int:
+        return self.heads * self.head_dim
+
+    def attention_flops(self) -> float:
+        """Counted work of one forward: 4 * S * I^2 * H * d (QK^T and PV)."""
+        return 4.0 * self.S * float(self.I) ** 2 * self.heads * self.head_dim
+
+
+MSA_WORKLOADS = {
+    "msa_tiny_f32": MsaWorkload("msa_tiny_f32", S=6, I=40, c_m=16, c_z=8, heads=2, head_dim=8, dtype="f32",
+                                n_pad=3, pad_rows=1, p_gap=0.1),
+    # Evoformer MSA stack shape: c_m = 256, c_z = 128, 8 heads of 32
+    "msa_evoformer_512": MsaWorkload("msa_evoformer_512", S=512, I=256, c_m=256, c_z=128, heads=8, head_dim=32,
+                                     dtype="bf16", n_pad=11, pad_rows=24, p_gap=0.1),
+}
+
+
+@dataclass
+class MsaInputs:
+    workload: MsaWorkload
+    Ms: np.ndarray             # [S, I, c_m] storage
+    Z: np.ndarray              # [I, I, c_z] storage
+    msa_mask: np.ndarray       # [S, I] uint8
+    w_q: np.ndarray            # [c_m, C]
+    w_k: np.ndarray
+    w_v: np.ndarray
+    w_g: np.ndarray
+    w_o: np.ndarray            # [C, c_m]
+    w_b: np.ndarray            # [c_z, H]
+    ln_m_gamma: np.ndarray
+    ln_m_beta: np.ndarray
+    ln_z_gamma: np.ndarray
+    ln_z_beta: np.ndarray
+    b_g: np.ndarray
+    b_o: np.ndarray
+
+    TENSORS = ("Ms", "Z", "w_q", "w_k", "w_v", "w_g", "w_o", "w_b", "ln_m_gamma", "ln_m_beta", "ln_z_gamma",
+               "ln_z_beta", "b_g", "b_o")
+
+    def widen(self, name: str) -> np.ndarray:
+        a = getattr(self, name)
+        if a.dtype == np.uint16:
+            return bf16_bits_to_f32(a).astype(np.float64)
+        return a.astype(np.float64)
+
+    def oracle_args(self) -> dict:
+        d = {n: self.widen(n) for n in self.TENSORS}
+        d["msa_mask"] = self.msa_mask.astype(bool)
+        return d
+
+
+def make_msa_inputs(wl: MsaWorkload | str, S: int | None = None, I: int | None = None) -> MsaInputs:
+    """Seeded inputs of an MSA workload (optionally with other S or I)."""
+    from dataclasses import replace
+    from .rng import uniform01
+    if isinstance(wl, str):
+        wl = MSA_WORKLOADS[wl]
+    if S is not None or I is not None:
+        S_, I_ = S or wl.S, I or wl.I
+        wl = replace(wl, S=S_, I=I_, n_pad=min(wl.n_pad, I_ // 8), pad_rows=min(wl.pad_rows, S_ // 4))
+    S, I, cm, cz, H, C, s = wl.S, wl.I, wl.c_m, wl.c_z, wl.heads, wl.C, wl.seed
+    ms = normal(s, STREAM_MSA, S * I * cm).reshape(S, I, cm).astype(np.float32)
+    z = normal(s, STREAM_MSA_Z, I * I * cz).reshape(I, I, cz).astype(np.float32)
+    mask = (uniform01(s, STREAM_MSA_MASK, 0, S * I).reshape(S, I) >= wl.p_gap).astype(np.uint8)
+    if wl.n_pad:
+        mask[:, I - wl.n_pad:] = 0
+    if wl.pad_rows:
+        mask[S - wl.pad_rows:] = 0
+    return MsaInputs(
+        workload=wl,
+        Ms=_store(ms, wl.dtype),
+        Z=_store(z, wl.dtype),
+        msa_mask=mask,
+        w_q=_store(_weight(s, STREAM_WQ, cm, C, cm), wl.dtype),
+        w_k=_store(_weight(s, STREAM_WK, cm, C, cm), wl.dtype),
+        w_v=_store(_weight(s, STREAM_WV, cm, C, cm), wl.dtype),
+        w_g=_store(_weight(s, STREAM_WG, cm, C, cm), wl.dtype),
+        w_o=_store(_weight(s, STREAM_WO, C, cm, C), wl.dtype),
+        w_b=_store(_weight(s, STREAM_WB, cz, H, cz), wl.dtype),
+        ln_m_gamma=np.ones(cm, dtype=np.float32),
+        ln_m_beta=np.zeros(cm, dtype=np.float32),
+        ln_z_gamma=np.ones(cz, dtype=np.float32),
+        ln_z_beta=np.zeros(cz, dtype=np.float32),
+        b_g=np.ones(C, dtype=np.float32),
+        b_o=np.zeros(cm, dtype=np.float32),
+    )

@@ -72,6 +72,13 @@ def test_null_arguments(lib):
     lib.tri_attn_destroy(None)
 
 
+def test_msa_entry_points_reject_null_arguments(lib):
+    w = B.MsaWeights()
+    assert lib.tri_attn_msa_workspace_bytes(None, 4, 8) == 0
+    assert lib.tri_attn_msa_forward(None, 4, 8, 16, 256, None, 512, ctypes.byref(w), 0, 1024, 1 << 20, 4096,
+                                    None) == B.EINVAL
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(FileNotFoundError):
         _load_missing(tmp_path)

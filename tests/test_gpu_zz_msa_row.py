@@ -1,0 +1,74 @@
+"""MSA row-wise gated attention with pair bias (tri_attn_msa_forward) against the
+fp64 oracle, through the C ABI on a GPU: f32 and bf16 storage, ragged residue
+counts, padded rows and gaps in the MSA mask, key chunks, the in-place residual,
+and sampled rows of the full Evoformer-shaped workload."""
+import numpy as np
+import pytest
+
+from oracle import msa_row_attention
+from tests.gpu_cases import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(name, S=None, I=None, key_chunks=1, residual=False, in_place=False):
+    import torch
+    import protein_pair_representation_gate_b300 as pkg
+    from synth import make_msa_inputs
+    from synth.device import msa_inputs_to_device
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    inp = make_msa_inputs(name, S=S, I=I)
+    wl = inp.workload
+    t = msa_inputs_to_device(inp, "cuda")
+    op = pkg.MSARowAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=key_chunks)
+    if in_place:
+        ms = t["Ms"].clone()
+        op(ms, t["Z"], t, msa_mask=t["msa_mask"], out=ms, residual=True)
+        out = ms
+    else:
+        out = op(t["Ms"], t["Z"], t, msa_mask=t["msa_mask"], residual=residual)
+    assert op.ctx.status_sync() == 0
+    return inp, out.float().cpu().numpy().astype(np.float64)
+
+
+def _want(inp, rows=None, residual=False):
+    a = inp.oracle_args()
+    return msa_row_attention(a["Ms"], a["Z"], a["msa_mask"], rows=rows, residual=residual,
+                             **{k: a[k] for k in ("w_q", "w_k", "w_v", "w_g", "w_b", "w_o", "ln_m_gamma",
+                                                  "ln_m_beta", "ln_z_gamma", "ln_z_beta", "b_g", "b_o")})
+
+
+def test_msa_f32():
+    inp, got = _run("msa_tiny_f32")
+    assert_close(got, _want(inp), "f32", "msa f32")
+    assert np.all(got[inp.msa_mask == 0] == 0.0)
+
+
+@pytest.mark.parametrize("S, I", [(8, 72), (5, 130)])
+def test_msa_bf16_evoformer_shape(S, I):
+    inp, got = _run("msa_evoformer_512", S=S, I=I)
+    assert_close(got, _want(inp), "bf16", f"msa bf16 S={S} I={I}")
+    assert np.all(got[inp.msa_mask == 0] == 0.0)
+
+
+def test_msa_key_chunks():
+    inp, got = _run("msa_evoformer_512", S=6, I=100, key_chunks=3)
+    assert_close(got, _want(inp), "bf16", "msa key chunks")
+
+
+def test_msa_residual_in_place_and_out_of_place():
+    inp, got = _run("msa_tiny_f32", residual=True)
+    assert_close(got, _want(inp, residual=True), "f32", "msa Ms + out")
+    inp, got = _run("msa_evoformer_512", S=6, I=72, in_place=True)
+    assert_close(got, _want(inp, residual=True), "bf16", "msa Ms += out")
+
+
+def test_msa_full_size_sampled_rows():
+    """The full msa_evoformer_512 workload (S = 512, I = 256), rows sampled for the
+    oracle: the first, a middle one, the last valid row and the last (padding) row."""
+    inp, got = _run("msa_evoformer_512")
+    S = inp.workload.S
+    rows = [0, 257, S - inp.workload.pad_rows - 1, S - 1]
+    assert_close(got[rows], _want(inp, rows=rows), "bf16", "msa full size")
+    assert np.all(got[S - inp.workload.pad_rows:] == 0.0)

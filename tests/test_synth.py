@@ -62,3 +62,19 @@ def test_block_diagonal_offset():
     assert abs(z.mean() - 2.0) < 0.05
     wl = WORKLOADS["complex_2048"]
     assert wl.chain_len == 256 and wl.block_offset == 2.0
+
+
+def test_msa_inputs_shapes_and_mask_structure():
+    from synth import make_msa_inputs
+    inp = make_msa_inputs("msa_evoformer_512", S=16, I=72)
+    wl = inp.workload
+    assert inp.Ms.shape == (16, 72, 256) and inp.Ms.dtype == np.uint16
+    assert inp.Z.shape == (72, 72, 128) and inp.w_b.shape == (128, 8) and inp.w_o.shape == (256, 256)
+    m = inp.msa_mask
+    assert m.shape == (16, 72) and m.dtype == np.uint8
+    assert not m[16 - wl.pad_rows:].any() and not m[:, 72 - wl.n_pad:].any()
+    gaps = 1.0 - m[:16 - wl.pad_rows, :72 - wl.n_pad].mean()
+    assert 0.0 < gaps < 0.25
+    again = make_msa_inputs("msa_evoformer_512", S=16, I=72)
+    np.testing.assert_array_equal(again.Ms, inp.Ms)
+    np.testing.assert_array_equal(again.msa_mask, inp.msa_mask)
