@@ -37,6 +37,7 @@
 // score contraction); OpenFold-TRT summary, Methodology: 16-bit core, fused
 // kernels; Design-CP summary, Methodology 1: key/value pieces with scores
 // formed on the fly and a log-sum-exp merge across key chunks.
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -1109,13 +1110,21 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+// SM count of the current device (cached per device)
 int num_sms() {
-    static int n = 0;
+    static std::atomic<int> cache[64];
+    const int dev = current_device();
+    int n = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
     if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (n <= 0) n = 148;
+        if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     }
     return n;
 }
@@ -1134,8 +1143,11 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
     const int I = a.I, Ip = a.I_pad;
 
-    static bool attr_done = false;
-    if (!attr_done) {
+    // the shared-memory opt-in is a per-device function attribute: set it once per device
+    static std::atomic<uint64_t> attr_set{0};
+    const int dev = current_device();
+    const uint64_t dev_bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (!(attr_set.load(std::memory_order_acquire) & dev_bit)) {
         cudaError_t e = cudaFuncSetAttribute(sm103_ln_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::kSmem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(sm103_attention<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1144,7 +1156,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         e = cudaFuncSetAttribute(sm103_attention<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  k2::Lay<true>::kSmem);
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        attr_set.fetch_or(dev_bit, std::memory_order_release);
     }
 
     // ---- weight preparation
