@@ -128,6 +128,21 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(value: float, pg, device) -> float:
+    """The largest of every rank's value: the job is as slow as its slowest rank."""
+    if pg is None:
+        return value
+    import torch
+    tt = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tflops(flops_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job rate: the work of all ranks (replicas) over the slowest rank's time."""
+    return flops_per_rank_step * steps * world / (ms * 1e-3) / 1e12
+
+
 class OracleSample:
     """The fp64 oracle on the host cores, on a bounded sample of one forward step.
 
@@ -288,13 +303,9 @@ def main():
     st = lib_ctx.status_sync(stream)
     if st != 0:
         raise RuntimeError(f"timed run failed: {pkg.status_string(st)}")
-    ms_total = e0.elapsed_time(e1)
-    if pg is not None:
-        tt = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), pg, dev)
     flops_step = 2 * wl.attention_flops()
-    value = flops_step * args.steps * world / (ms_total * 1e-3) / 1e12
+    value = job_tflops(flops_step, args.steps, world, ms_total)
 
     # dominant kernel: largest total time
     dom = max(kernel_ms, key=lambda k: sum(kernel_ms[k]))
@@ -359,12 +370,9 @@ def main():
         st = lib_ctx.status_sync(stream)
         if st != 0:
             raise RuntimeError(f"end-to-end run failed: {pkg.status_string(st)}")
-        if pg is not None:
-            tt = torch.tensor([ms_e2e], device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
+        ms_e2e = max_over_ranks(ms_e2e, pg, dev)
         nb = hz.numel() * hz.element_size()
-        e2e = {"value": flops_step * k * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_tflops(flops_step, k, world, ms_e2e), "unit": UNIT,
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": 2 * nb, "ms_per_step": ms_e2e / k,
                "copies": "pinned host buffers, own streams, double-buffered across steps"}
 
