@@ -28,9 +28,13 @@
 //                   against an identity), online softmax with lazy rescaling,
 //                   P (f16) written back into TMEM over S, O += P V (A operand
 //                   from TMEM), then normalise, gate, and the output projection
-//                   (u W_o, A operand from TMEM) with the pair mask, stored in
+//                   (u W_o, A operand from TMEM) with the token mask, stored in
 //                   the node's orientation.  The I x I score matrix of a line
-//                   is never materialised.
+//                   is never materialised.  A second build of this kernel
+//                   serves calls with an [I, I] pair mask (one more K-step adds
+//                   -30000 on the line's excluded keys) or a residual (Z + out).
+//   sm103_pair_keybits  (with a pair mask only) packs each line's admitted
+//                   keys into 64-bit words for the attention kernel.
 //
 // Sources: the operation as stated in tri_attn.h (Dell page, Evoformer
 // paragraph; Intel page, steps 2 and 4: bias term and fusing it into the
