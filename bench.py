@@ -6,7 +6,12 @@ seeded large-complex pair tensor (Z ~ N(0,1) + 2.0 on 8 diagonal chain
 blocks of 256 tokens, bf16).  Counted work per forward: 4 * I^3 * H * d.
 Inputs (Z = 1 GiB) are larger than L2, so no flush is needed between steps.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--chained]
+
+--chained times the Evoformer's own call pattern instead: each step updates
+the pair tensor in place, Z += start(Z) then Z += end(Z), through the residual
+entry point (the same counted work; one tensor in and one out per step end to
+end).
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 (the path has no cross-GPU exchange); value = all ranks' work / max time.
@@ -39,6 +44,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--force-simt", action="store_true")
+    ap.add_argument("--chained", action="store_true")
     return ap.parse_args()
 
 
@@ -272,10 +278,19 @@ def main():
     lib_ctx = op.ctx
     out = {node: torch.empty_like(t["Z"]) for node in ("start", "end")}
     stream = torch.cuda.current_stream(dev)
+    chained = args.chained
+    zw = t["Z"].clone() if chained else t["Z"]        # chained: the pair tensor updated in place
+
+    def forward_step(z, outs, strm):
+        if chained:
+            for node in ("start", "end"):
+                op(node, z, t, mask=t["mask"], out=z, stream=strm, residual=True)
+        else:
+            for node in ("start", "end"):
+                op(node, z, t, mask=t["mask"], out=outs[node], stream=strm)
 
     def step():
-        for node in ("start", "end"):
-            op(node, t["Z"], t, mask=t["mask"], out=out[node], stream=stream)
+        forward_step(zw, out, stream)
 
     for _ in range(args.warmup):
         step()
@@ -292,8 +307,7 @@ def main():
     with ClockSampler(local) as clk:
         e0.record(stream)
         for _ in range(args.steps):
-            for node in ("start", "end"):
-                op(node, t["Z"], t, mask=t["mask"], out=out[node], stream=stream)
+            forward_step(zw, out, stream)
         e1.record(stream)
         barrier()
     for name, ms in lib_ctx.kernel_times():
@@ -327,7 +341,7 @@ def main():
     e2e = None
     if not args.no_e2e:
         hz = t["Z"].cpu().pin_memory()
-        nodes = ("start", "end")
+        nodes = ("z",) if chained else ("start", "end")
         hout = [{n: torch.empty(hz.shape, dtype=hz.dtype).pin_memory() for n in nodes} for _ in range(2)]
         dz = [torch.empty_like(t["Z"]) for _ in range(2)]
         dout = [{n: torch.empty_like(t["Z"]) for n in nodes} for _ in range(2)]
@@ -345,18 +359,19 @@ def main():
                 with torch.cuda.stream(s_in):
                     if i >= 2:
                         s_in.wait_event(comp_done[i - 2])      # dz[b] is free again
+                        if chained:
+                            s_in.wait_event(out_done[i - 2])   # ... and its result read back
                     dz[b].copy_(hz, non_blocking=True)
                     in_done[i].record(s_in)
                 stream.wait_event(in_done[i])
                 if i >= 2:
                     stream.wait_event(out_done[i - 2])          # dout[b] has been read back
-                for node in nodes:
-                    op(node, dz[b], t, mask=t["mask"], out=dout[b][node], stream=stream)
+                forward_step(dz[b], dout[b], stream)
                 comp_done[i].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(comp_done[i])
                     for node in nodes:
-                        hout[b][node].copy_(dout[b][node], non_blocking=True)
+                        hout[b][node].copy_(dz[b] if chained else dout[b][node], non_blocking=True)
                     out_done[i].record(s_out)
 
         run(0, 2)                                               # warm-up
@@ -373,7 +388,7 @@ def main():
         ms_e2e = max_over_ranks(ms_e2e, pg, dev)
         nb = hz.numel() * hz.element_size()
         e2e = {"value": job_tflops(flops_step, k, world, ms_e2e), "unit": UNIT,
-               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": 2 * nb, "ms_per_step": ms_e2e / k,
+               "h2d_bytes_per_step": nb, "d2h_bytes_per_step": len(nodes) * nb, "ms_per_step": ms_e2e / k,
                "copies": "pinned host buffers, own streams, double-buffered across steps"}
 
     cpu = None
@@ -390,6 +405,8 @@ def main():
                                        "starting + ending node per step",
                            "I": wl.I, "c_z": wl.c_z, "heads": wl.heads, "head_dim": wl.head_dim,
                            "path": ["simt", "sm103"][op.path], "l2": "inputs larger than L2 (Z = 1 GiB); no flush",
+                           "step": ("Z += start(Z); Z += end(Z), in place (residual)" if chained
+                                    else "start(Z) and end(Z), update only"),
                            "parallelism": f"replicas x{world}"},
                 "frac_of_peak": value / peak, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clocks,
