@@ -132,8 +132,10 @@ size_t tri_attn_workspace_bytes(const tri_attn_ctx* ctx, int I);
  *   Z           [I, I, c_z] dtype, row-major, 16-byte aligned
  *   token_mask  [I] uint8 (nonzero = valid token), or NULL for all valid
  *   w           module parameters (struct itself is host memory)
- *   workspace   >= tri_attn_workspace_bytes(ctx, I) bytes, 256-byte aligned
- *   out         [I, I, c_z] dtype, 16-byte aligned, must not overlap Z or the workspace
+ *   workspace   >= tri_attn_workspace_bytes(ctx, I) bytes, 256-byte aligned; must
+ *               not overlap Z, token_mask or out
+ *   out         [I, I, c_z] dtype, 16-byte aligned, must not overlap Z, token_mask
+ *               or the workspace
  *   stream      cudaStream_t as void*
  * Writes out (the update only).  Asynchronous; returns EINVAL / EUNSUPPORTED
  * / ENOMEM from validation without launching, ECUDA if a launch fails. */
@@ -217,7 +219,8 @@ size_t tri_attn_msa_workspace_bytes(const tri_attn_ctx* ctx, int S, int I);
  *   Z           [I, I, cfg.c_z] dtype, row-major, 16-byte aligned
  *   w           parameters (struct itself is host memory; device pointers)
  *   residual    nonzero: write Ms + update; out may then be msa itself
- *   workspace   >= tri_attn_msa_workspace_bytes(ctx, S, I) bytes, 256-byte aligned
+ *   workspace   >= tri_attn_msa_workspace_bytes(ctx, S, I) bytes, 256-byte aligned;
+ *               must not overlap msa, msa_mask, Z or out
  *   out         [S, I, c_m] dtype, 16-byte aligned; must not overlap Z, the
  *               workspace or msa_mask, nor msa unless it is msa itself with residual
  *               (msa_mask must not lie in the workspace either)

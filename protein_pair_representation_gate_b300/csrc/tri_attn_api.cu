@@ -160,7 +160,10 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* c, int node, int I, const void
     const size_t pair_bytes = (size_t)I * I * g.c_z * esz;
     const bool residual = opt && opt->residual;
     const bool in_place = residual && out == Z;          // the one overlap allowed: Z += update
-    if ((!in_place && overlaps(out, pair_bytes, Z, pair_bytes)) || overlaps(out, pair_bytes, workspace, lay.total))
+    if ((!in_place && overlaps(out, pair_bytes, Z, pair_bytes)) || overlaps(out, pair_bytes, workspace, lay.total) ||
+        overlaps(Z, pair_bytes, workspace, lay.total))
+        return TRI_ATTN_EINVAL;
+    if (mask && (overlaps(mask, (size_t)I, out, pair_bytes) || overlaps(mask, (size_t)I, workspace, lay.total)))
         return TRI_ATTN_EINVAL;
     const uint8_t* pmask = opt ? opt->pair_mask : nullptr;
     if (pmask && (overlaps(pmask, (size_t)I * I, out, pair_bytes) || overlaps(pmask, (size_t)I * I, workspace, lay.total)))
@@ -223,7 +226,8 @@ tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, con
     const size_t msa_bytes = (size_t)S * I * c_m * esz, z_bytes = (size_t)I * I * g.c_z * esz;
     const bool in_place = residual && out == msa;        // the one overlap allowed: Ms += update
     if ((!in_place && overlaps(out, msa_bytes, msa, msa_bytes)) || overlaps(out, msa_bytes, Z, z_bytes) ||
-        overlaps(out, msa_bytes, workspace, lay.total))
+        overlaps(out, msa_bytes, workspace, lay.total) || overlaps(msa, msa_bytes, workspace, lay.total) ||
+        overlaps(Z, z_bytes, workspace, lay.total))
         return TRI_ATTN_EINVAL;
     if (msa_mask && (overlaps(msa_mask, (size_t)S * I, out, msa_bytes) ||
                      overlaps(msa_mask, (size_t)S * I, workspace, lay.total)))
