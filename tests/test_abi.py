@@ -91,3 +91,20 @@ def _load_missing(tmp_path):
         B.load_library(str(tmp_path / "missing.so"))
     finally:
         B._lib = saved
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/tri_attn.h compiles as C99 (no C++ in the ABI) and declares every
+    exported entry point with a prototype a C caller can take the address of."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    names = sorted(declared_functions())
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "tri_attn.h"\nvoid* entry_points[] = {\n' +
+                   "".join(f"    (void*){n},\n" for n in names) + "};\n")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
