@@ -108,3 +108,16 @@ def test_header_is_plain_c(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_no_cpu_fallback_without_a_gpu(lib):
+    """Without a CUDA device the product path fails loudly: creating a context
+    (triangle or MSA) raises instead of computing anything on the host."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    with pytest.raises(B.TriAttnError) as e:
+        pkg.TriangleAttention(128, 4, 32, 64, "bf16")
+    assert e.value.status in (B.ECUDA, B.EUNSUPPORTED)
+    with pytest.raises(B.TriAttnError):
+        pkg.MSARowAttention(128, 8, 32, 64, "bf16")
