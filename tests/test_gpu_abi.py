@@ -57,8 +57,10 @@ def test_validation_launches_nothing(setup):
         dict(out=ws.data_ptr()),
         dict(weights={**t, "w_q": None}),
         dict(weights={**t, "w_o": t["w_o"].data_ptr() + 2}),
+        dict(Z=ws.data_ptr()),                 # input inside the workspace
+        dict(mask=out.data_ptr()),             # token mask inside the output
     ]
-    want = [B.EINVAL] * 6 + [B.ENOMEM] + [B.EINVAL] * 4
+    want = [B.EINVAL] * 6 + [B.ENOMEM] + [B.EINVAL] * 6
     for kw, st in zip(cases, want):
         args = dict(node=0, I=64, Z=Z, mask=t["mask"], weights=t, workspace=ws, out=out, workspace_bytes=nbytes)
         args.update(kw)
