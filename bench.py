@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--force-simt", action="store_true")
     ap.add_argument("--chained", action="store_true")
     return ap.parse_args()
@@ -149,15 +150,31 @@ def job_tflops(flops_per_rank_step: float, steps: int, world: int, ms: float) ->
     return flops_per_rank_step * steps * world / (ms * 1e-3) / 1e12
 
 
+def sample_lines(wl, n_random: int = 16, seed: int = 0) -> list[int]:
+    """The oracle's line sample of one node: the first and the last line, both
+    sides of every chain boundary (workloads built from chains), and n_random
+    seeded-random other lines."""
+    import numpy as np
+    I = wl.I
+    chosen = {0, I - 1}
+    if wl.chain_len:
+        for b in range(wl.chain_len, I, wl.chain_len):
+            chosen.update((b - 1, b))
+    rest = np.array(sorted(set(range(I)) - chosen))
+    rng = np.random.default_rng(seed)
+    extra = rng.choice(rest, size=min(n_random, len(rest)), replace=False) if len(rest) else []
+    return sorted(chosen | {int(x) for x in extra})
+
+
 class OracleSample:
     """The fp64 oracle on the host cores, on a bounded sample of one forward step.
 
-    A step is a starting- and an ending-node forward; the oracle computes the
-    pair bias over all I x I pairs once per node and then each line (row for
-    the starting node, column for the ending node) independently.  The full
-    pair-bias pass is timed once; each sample then times `lines` random rows
-    and columns, and the step time is extrapolated as
-    2 * t_bias + I * (t_row + t_col)."""
+    A step is a starting- and an ending-node forward.  The oracle computes the
+    pair bias over all I x I pairs once per node, then each line (row for the
+    starting node, column for the ending node) independently given that bias,
+    so a step's time is estimated as 2 * t_bias + I * (mean t_row + mean t_col)
+    from the full pair-bias pass (timed) and the lines of `sample_lines`
+    (each timed once per node)."""
 
     def __init__(self, wl_name: str):
         from oracle import pair_bias
@@ -169,42 +186,42 @@ class OracleSample:
         t0 = time.perf_counter()
         self.bias = pair_bias(self.a["Z"], self.a["ln_gamma"], self.a["ln_beta"], self.a["w_b"])
         self.t_bias = time.perf_counter() - t0
-        self.calls = 0
+        self.lines = sample_lines(self.wl)
+        self.times = {"start": [], "end": []}
 
-    def step(self, lines: int = 2):
-        """One sampled step: returns (extrapolated seconds per step, description)."""
-        import numpy as np
+    def time_line(self, node: str, line: int) -> float:
         from oracle import triangle_attention
+        t1 = time.perf_counter()
+        triangle_attention(node, self.a["Z"], self.a["mask"], self.a, lines=[line], bias=self.bias)
+        dt = time.perf_counter() - t1
+        self.times[node].append(dt)
+        return dt
 
-        rng = np.random.default_rng(self.calls)
-        self.calls += 1
-        per = {}
-        for node in ("start", "end"):
-            t_sum = 0.0
-            for _ in range(lines):
-                line = [int(rng.integers(0, self.wl.I))]
-                t1 = time.perf_counter()
-                triangle_attention(node, self.a["Z"], self.a["mask"], self.a, lines=line, bias=self.bias)
-                t_sum += time.perf_counter() - t1
-            per[node] = t_sum / lines
-        t_step = 2 * self.t_bias + self.wl.I * (per["start"] + per["end"])
-        desc = (f"fp64 numpy oracle, {self.wl.name}: pair bias over all {self.wl.I}x{self.wl.I} pairs timed once "
-                f"({self.t_bias:.1f} s) + {lines} starting-node rows and {lines} ending-node columns "
-                f"({per['start']:.2f} s, {per['end']:.2f} s each); step = 2*t_bias + I*(t_row + t_col) "
-                f"= {t_step:.0f} s, extrapolated")
-        return t_step, desc
+    def estimate(self) -> float:
+        """Seconds per step from every line timed so far."""
+        mean = {n: statistics.fmean(v) for n, v in self.times.items()}
+        return 2 * self.t_bias + self.wl.I * (mean["start"] + mean["end"])
+
+    def describe(self) -> str:
+        n = {k: len(v) for k, v in self.times.items()}
+        return (f"fp64 numpy oracle, {self.wl.name}: pair bias over all {self.wl.I}x{self.wl.I} pairs timed once "
+                f"({self.t_bias:.1f} s); {n['start']} starting-node rows and {n['end']} ending-node columns timed "
+                f"(mean {statistics.fmean(self.times['start']):.3f} s and {statistics.fmean(self.times['end']):.3f} s) "
+                f"from a sample of {len(self.lines)} lines per node (first, last, both sides of every chain boundary, "
+                f"16 seeded-random lines); step = 2*t_bias + I*(t_row + t_col) = {self.estimate():.0f} s, "
+                f"extrapolated")
 
 
-def cpu_baseline(wl_name: str, samples: int = 4):
-    """cpu_baseline object of the bench line: the oracle as it stands, on a bounded sample."""
+def cpu_baseline(wl_name: str):
+    """cpu_baseline object of the bench line: the oracle as it stands, on the line sample."""
     o = OracleSample(wl_name)
-    times = []
-    for _ in range(samples):
-        t, desc = o.step(lines=2)
-        times.append(t)
-    t_step = statistics.median(times)
+    for line in o.lines:
+        for node in ("start", "end"):
+            o.time_line(node, line)
+    t_step = o.estimate()
     return {"value": 2 * o.wl.attention_flops() / t_step / 1e12, "unit": UNIT, "cores": _blas_threads(),
-            "kind": "oracle", "sample": desc + f"; median of {samples} samples"}
+            "kind": "oracle", "sample": o.describe(), "extrapolated": True,
+            "lines_timed": len(o.times["start"]) + len(o.times["end"])}
 
 
 def _blas_threads():
@@ -217,24 +234,35 @@ def _blas_threads():
 
 
 def run_reference(args, world, rank):
-    """Reference arm: the oracle on the host cores (rank 0 only), same metric and config."""
+    """Reference arm: the oracle on the host cores (rank 0 only), same metric and config.
+
+    Each step times one row and one column of the line sample (in turn); the
+    reported step time is the estimate from every line timed in the K steps
+    (the warm-up steps time lines too, outside the reported count)."""
     if rank != 0:
         return
     t0 = time.perf_counter()
     o = OracleSample(args.workload)
     wl = o.wl
-    for _ in range(args.warmup and 1):
-        o.step(lines=1)
-    times, desc = [], ""
+    order = o.lines
+    k = 0
+    for _ in range(args.warmup):
+        line = order[k % len(order)]
+        o.time_line("start", line)
+        o.time_line("end", line)
+        k += 1
+    o.times = {"start": [], "end": []}
     for _ in range(max(1, args.steps)):
-        t, desc = o.step(lines=1)
-        times.append(t)
-    t_step = statistics.median(times)
+        line = order[k % len(order)]
+        o.time_line("start", line)
+        o.time_line("end", line)
+        k += 1
+    t_step = o.estimate()
     value = 2 * wl.attention_flops() / t_step / 1e12
-    cb = {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
-          "sample": desc + f"; median of {len(times)} sampled steps"}
+    cb = {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle", "sample": o.describe(),
+          "extrapolated": True, "lines_timed": len(o.times["start"]) + len(o.times["end"])}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "extrapolated": True,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded SplitMix64/Box-Muller), same inputs as the GPU arm",
             "config": {"workload": f"{args.workload}: I={wl.I}, c_z={wl.c_z}, H={wl.heads}, d={wl.head_dim}, "
@@ -244,6 +272,66 @@ def run_reference(args, world, rank):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t0}
     print(json.dumps(line), flush=True)
+
+
+def secondary_runs(pkg, dev, peak):
+    """Timings of the other workloads (parity-test configurations), outside the timed region:
+    per forward, CUDA events around the library call, after warm-up."""
+    import numpy as np
+    import torch
+    from synth import make_inputs
+    from synth.device import inputs_to_device
+    from synth.rng import uniform01
+
+    cases = [("masked_768", ("start", "end"), 1, None, 5),
+             ("single_chain_2752", ("start",), 1, None, 3),
+             ("single_chain_2752", ("start",), 8, None, 3),
+             ("complex_2048", ("start", "end"), 1, 0.8, 3)]
+    res = []
+    for name, nodes, chunks, density, iters in cases:
+        inp = make_inputs(name)
+        wl = inp.workload
+        t = inputs_to_device(inp, dev)
+        op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=chunks)
+        pm = None
+        if density is not None:
+            u = uniform01(wl.seed, 13, 0, wl.I * wl.I).reshape(wl.I, wl.I)
+            pm = torch.from_numpy((u < density).astype(np.uint8)).to(dev)
+        out = torch.empty_like(t["Z"])
+        stream = torch.cuda.current_stream(dev)
+
+        def one():
+            for node in nodes:
+                op(node, t["Z"], t, mask=t["mask"], out=out, pair_mask=pm, stream=stream)
+
+        for _ in range(2):
+            one()
+        op.ctx.set_timing(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        kms = {}
+        for kname, ms in op.ctx.kernel_times():
+            kms.setdefault(kname, []).append(ms)
+        op.ctx.set_timing(False)
+        st = op.ctx.status_sync(stream)
+        if st != 0:
+            raise RuntimeError(f"{name}: {pkg.status_string(st)}")
+        ms_fwd = e0.elapsed_time(e1) / (iters * len(nodes))
+        tf = wl.attention_flops() / (ms_fwd * 1e-3) / 1e12
+        att = sum(kms.get("sm103_attention", [0.0])) / (iters * len(nodes))
+        res.append({"workload": name, "I": wl.I, "nodes": list(nodes), "key_chunks": chunks,
+                    "pair_mask_density": density, "token_pads": wl.n_pad, "ms_per_forward": ms_fwd,
+                    "tflops": tf, "frac_of_peak": tf / peak,
+                    "attention_ms_per_forward": att,
+                    "kernels_ms_per_forward": {k: sum(v) / (iters * len(nodes)) for k, v in kms.items()}})
+        del t, op, out, pm
+        torch.cuda.empty_cache()
+    return res
 
 
 def main():
@@ -391,6 +479,10 @@ def main():
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": len(nodes) * nb, "ms_per_step": ms_e2e / k,
                "copies": "pinned host buffers, own streams, double-buffered across steps"}
 
+    secondary = None
+    if not args.no_secondary:
+        secondary = secondary_runs(pkg, dev, peaks()[0])
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload)
@@ -409,7 +501,7 @@ def main():
                                     else "start(Z) and end(Z), update only"),
                            "parallelism": f"replicas x{world}"},
                 "frac_of_peak": value / peak, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clocks,
+                "gpu_launches": launches, "clocks": clocks, "secondary": secondary,
                 "kernels_ms": {k: sum(v) / len(v) for k, v in kernel_ms.items()}}
         print(json.dumps(line), flush=True)
     if pg is not None:

@@ -65,7 +65,9 @@ typedef enum {
     TRI_ATTN_EUNSUPPORTED = 2,  /* shape or dtype the library has no kernel for          */
     TRI_ATTN_ENOMEM = 3,        /* workspace too small, or host allocation failed        */
     TRI_ATTN_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed           */
-    TRI_ATTN_ETIMEOUT = 5       /* a device-side bounded wait gave up (status word set)  */
+    TRI_ATTN_ETIMEOUT = 5,      /* a device-side bounded wait gave up (status word set)  */
+    TRI_ATTN_ERANGE = 6         /* an f16 intermediate of the sm103 path (q, k, v or the */
+                                /* pair bias) left the f16 range: the output is invalid  */
 } tri_attn_status;
 
 typedef enum { TRI_ATTN_STARTING = 0, TRI_ATTN_ENDING = 1 } tri_attn_node;
@@ -234,7 +236,10 @@ tri_attn_status tri_attn_msa_forward(tri_attn_ctx* ctx, int S, int I, int c_m,
 
 /* Synchronise `stream`, then read and clear the context's device status word.
  * Returns ETIMEOUT if a kernel gave up a bounded wait since the last call,
- * ECUDA if the stream reports an error, else OK. */
+ * else ERANGE if a forward on the sm103 path met a non-finite value (one of its
+ * f16 intermediates q, k, v or pair bias exceeded 65504 in magnitude, e.g. from
+ * LayerNorm weights far beyond a trained model's scale), ECUDA if the stream
+ * reports an error, else OK. */
 tri_attn_status tri_attn_status_sync(tri_attn_ctx* ctx, void* stream);
 
 /* Per-kernel timing.  tri_attn_set_timing(ctx, 1) clears the record list and
@@ -263,18 +268,29 @@ int tri_attn_kernel_times(tri_attn_ctx* ctx, const char** names, float* ms, int 
  *               (the sm103 kernels; sm_103 devices only, else EUNSUPPORTED)
  *   I           1 <= I <= 128; larger I returns TRI_ATTN_EUNSUPPORTED
  *   ln_eps      LayerNorm epsilon, 0 < ln_eps <= 1
- *   other args  as for tri_attn_forward (device pointers, 16-byte aligned;
- *               out must not overlap Z)
- * It calls no cudaMalloc, cudaFree or other allocating routine.  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current) and caches it: make that first call before any
- * stream capture.  Every call shares the one array and leaves its contents
- * behind; the status word inside it is cleared at the start of each call, and
- * a device-side wait that gives up leaves `out` incomplete without being
- * reported here.  Calls whose work overlaps on the GPU race on the array:
- * issue them on one stream, or otherwise order them. */
+ *   other args  as for tri_attn_forward (device pointers, 16-byte aligned);
+ *               out must not overlap Z or token_mask, and none of Z, token_mask
+ *               and out may lie in the library's array (EINVAL, nothing launched)
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The array's
+ * device address belongs to the CUDA context current at the call: the first
+ * call in each context (per device, and again after cudaDeviceReset re-creates
+ * the primary context) looks it up with cudaGetSymbolAddress and caches it
+ * under the context's id, so make that first call before any stream capture.
+ * Every call shares the one array and leaves its contents behind; the status
+ * word inside it is cleared (on the stream) at the start of each call.  Calls
+ * whose work overlaps on the GPU race on the array: issue them on one stream,
+ * or otherwise order them. */
 tri_attn_status tri_attn_forward_static(int node, int I, const void* Z, const uint8_t* token_mask,
                                         const tri_attn_weights* w, float ln_eps, void* out, void* stream);
+
+/* Status of the last tri_attn_forward_static on the current device, without
+ * allocating: synchronises `stream`, reads the status word in the library's
+ * array and clears it.  Returns ETIMEOUT if a device-side bounded wait of that
+ * call gave up (its `out` is then incomplete), else ERANGE if an f16
+ * intermediate left the f16 range (as for tri_attn_status_sync), ECUDA if the
+ * stream or the copy reports an error, else OK.  Call it before the next static call (which clears
+ * the word). */
+tri_attn_status tri_attn_static_status(void* stream);
 
 /* Test hook for the failure path (no GPU fault is involved).
  * fault = TRI_ATTN_FAULT_SKIP_STAGE: the next tri_attn_forward of this context
@@ -286,6 +302,11 @@ tri_attn_status tri_attn_forward_static(int node, int I, const void* Z, const ui
  * forward; fault = 0 clears it.  EUNSUPPORTED on the SIMT path. */
 enum { TRI_ATTN_FAULT_NONE = 0, TRI_ATTN_FAULT_SKIP_STAGE = 1 };
 tri_attn_status tri_attn_debug_inject(tri_attn_ctx* ctx, int fault);
+
+/* The same test hook for tri_attn_forward_static: the next static call (in this
+ * process) runs with the first block's producer skipping one stage load;
+ * tri_attn_static_status then returns TRI_ATTN_ETIMEOUT.  fault = 0 clears it. */
+tri_attn_status tri_attn_static_debug_inject(int fault);
 
 /* Static description of a status code. */
 const char* tri_attn_status_string(int status);

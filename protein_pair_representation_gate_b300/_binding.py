@@ -13,7 +13,7 @@ from dataclasses import dataclass
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libtriattn.so")
 
-OK, EINVAL, EUNSUPPORTED, ENOMEM, ECUDA, ETIMEOUT = range(6)
+OK, EINVAL, EUNSUPPORTED, ENOMEM, ECUDA, ETIMEOUT, ERANGE = range(7)
 STARTING, ENDING = 0, 1
 F32, BF16 = 0, 1
 PATH_SIMT, PATH_SM103 = 0, 1
@@ -22,7 +22,8 @@ NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
 EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
            "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
            "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject", "tri_attn_forward_ex",
-           "tri_attn_msa_workspace_bytes", "tri_attn_msa_forward")
+           "tri_attn_msa_workspace_bytes", "tri_attn_msa_forward", "tri_attn_static_status",
+           "tri_attn_static_debug_inject")
 FAULT_NONE, FAULT_SKIP_STAGE = 0, 1
 
 
@@ -91,6 +92,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tri_attn_kernel_times.restype = i
     lib.tri_attn_forward_static.argtypes = [i, i, vp, vp, ctypes.POINTER(Weights), ctypes.c_float, vp, vp]
     lib.tri_attn_forward_static.restype = i
+    lib.tri_attn_static_status.argtypes = [vp]
+    lib.tri_attn_static_status.restype = i
+    lib.tri_attn_static_debug_inject.argtypes = [i]
+    lib.tri_attn_static_debug_inject.restype = i
     lib.tri_attn_debug_inject.argtypes = [vp, i]
     lib.tri_attn_debug_inject.restype = i
     lib.tri_attn_status_string.argtypes = [i]
@@ -142,6 +147,16 @@ def forward_static(node, I: int, Z, mask, weights: dict, out, ln_eps: float = 1e
     w = Weights(*[_ptr(weights.get(n)) for n, _ in Weights._fields_])
     return lib.tri_attn_forward_static(NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(w), ln_eps,
                                        _ptr(out), _stream_ptr(stream))
+
+
+def static_status(stream=None) -> int:
+    """tri_attn_static_status: synchronise the stream, read and clear the static path's status word."""
+    return load_library().tri_attn_static_status(_stream_ptr(stream))
+
+
+def static_debug_inject(fault: int) -> int:
+    """tri_attn_static_debug_inject: the next forward_static runs with the stage-skip test hook."""
+    return load_library().tri_attn_static_debug_inject(fault)
 
 
 class TriAttn:

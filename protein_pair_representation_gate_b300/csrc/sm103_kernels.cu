@@ -623,6 +623,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             prefetch_tmap(&mapB);
         }
         bool ok = true;
+        int it_issued = 0, skipped = -1, q_loads = 0;   // for the drain on the abort path
         if (leader && p.last) {                   // W_o^T for the output projection at the block end
             prefetch_tmap(&mapWo);
             mbar_arrive_expect_tx(w_full, 32768);
@@ -642,6 +643,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
                         tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
                     }
+                    q_loads = h + 1;
                 }
                 uint32_t two = 0;                 // key-valid bits of keys k0 + 2 lane, + 1 (read before the wait;
                 if (kEx && p.kbits != nullptr) {  // k0 is a multiple of 8, so both bits sit in one 32-bit word)
@@ -669,6 +671,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
                     tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
                 }
+                if (skip) skipped = it;
+                it_issued = it + 1;
                 __syncwarp();
             }
         }
@@ -678,7 +682,22 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             volatile int keep_waiting = 0;
             mbar_wait(w_full, 0, &keep_waiting);
         }
-        if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
+        if (!ok) {
+            // gave up (or another role did): before the block ends, wait (bounded,
+            // ignoring the abort flag) for the last copy issued into each K / V' stage
+            // and each Q buffer, so that no TMA write lands in freed shared memory
+            if (leader) set_abort(abort, p.status, kStatusTimeoutProducer);
+            volatile int keep_waiting = 0;
+            for (int st = 0; st < k2::kStages; ++st) {
+                int j = it_issued - 1 - ((it_issued - 1 - st) % k2::kStages + k2::kStages) % k2::kStages;
+                if (j == skipped) j -= k2::kStages;
+                if (j >= 0) mbar_wait(kv_full + st, (j / k2::kStages) & 1, &keep_waiting);
+            }
+            for (int b = 0; b < 2; ++b) {
+                const int hl = q_loads - 1 - ((q_loads - 1 - b) % 2 + 2) % 2;   // last head loaded into buffer b
+                if (hl >= 0) mbar_wait(q_full + b, (hl >> 1) & 1, &keep_waiting);
+            }
+        }
     } else if (warp == 1 || warp == 2) {
         setmaxnreg_dec<120>();
         // ------------------------------------------------------------ MMA issuers
@@ -835,7 +854,19 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 else __nanosleep(64);
             }
         }
-        if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutProducer);
+        if (!ok) {
+            // gave up: before the block ends, wait (bounded, ignoring the abort flag) for
+            // the last bias copy issued into each stage of both rings
+            if (leader) set_abort(abort, p.status, kStatusTimeoutProducer);
+            volatile int keep_waiting = 0;
+            for (int g = 0; g < 2; ++g) {
+                const int issued = g ? nb1 : nb0;
+                for (int st = 0; st < k2::kBStages; ++st) {
+                    const int j = issued - 1 - ((issued - 1 - st) % k2::kBStages + k2::kBStages) % k2::kBStages;
+                    if (j >= 0) mbar_wait(b_full + g * k2::kBStages + st, (j / k2::kBStages) & 1, &keep_waiting);
+                }
+            }
+        }
     } else if (warp < 4) {
         setmaxnreg_dec<120>();                     // idle warps of the control warpgroup
     } else {
@@ -867,8 +898,16 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             float o[HD];
             const float inv = l > 0.f ? 1.f / l : 0.f;
             float lse = l > 0.f ? m + __log2f(l) : -INFINITY;
+            // an f16 intermediate (q, k, v, pair bias) out of range shows up here as a
+            // non-finite row sum or output (a NaN or an infinity anywhere makes the sum
+            // non-finite): latch it in the status word.  Rows past I are padding.
+            float chk = l;
 #pragma unroll
-            for (int e = 0; e < HD; ++e) o[e] = __uint_as_float(ov[e]) * inv;
+            for (int e = 0; e < HD; ++e) {
+                o[e] = __uint_as_float(ov[e]) * inv;
+                chk += fabsf(o[e]);
+            }
+            if (x < p.I && !(chk < INFINITY)) atomicOr(p.status, kStatusRange);
             const size_t srow = ((size_t)(L * NH + hp)) * p.I_pad + x;
             if (!p.first) {
                 const float lr = p.lse_run[srow];

@@ -337,20 +337,12 @@ __device__ __forceinline__ uint32_t exp2_pair_f16x2(float a, float b, float negm
         : "f"(a), "f"(b), "f"(negm));
     return r;
 }
-// same with two f32 exp2 and a rounding pack (more accurate, twice the MUFU work)
-__device__ __forceinline__ uint32_t exp2_pair_f32(float a, float b, float negm) {
-    uint32_t r;
-    asm("{\n\t.reg .b64 x, y, n;\n\t.reg .f32 lo, hi, elo, ehi;\n\t"
-        "mov.b64 x, {%1, %2};\n\tmov.b64 n, {%3, %3};\n\t"
-        "add.rn.f32x2 y, x, n;\n\tmov.b64 {lo, hi}, y;\n\t"
-        "ex2.approx.ftz.f32 elo, lo;\n\tex2.approx.ftz.f32 ehi, hi;\n\t"
-        "cvt.rn.f16x2.f32 %0, ehi, elo;\n\t}"
-        : "=r"(r)
-        : "f"(a), "f"(b), "f"(negm));
-    return r;
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// generic-proxy writes to global memory made visible to later async-proxy (TMA) reads
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

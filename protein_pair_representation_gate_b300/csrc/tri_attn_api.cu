@@ -83,6 +83,7 @@ const char* tri_attn_status_string(int s) {
         case TRI_ATTN_ENOMEM: return "workspace too small or allocation failed";
         case TRI_ATTN_ECUDA: return "CUDA error";
         case TRI_ATTN_ETIMEOUT: return "device wait timed out";
+        case TRI_ATTN_ERANGE: return "f16 intermediate out of range";
         default: return "unknown status";
     }
 }
@@ -269,7 +270,7 @@ tri_attn_status tri_attn_status_sync(tri_attn_ctx* c, void* stream) {
     if (cudaMemcpy(&v, c->d_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return TRI_ATTN_ECUDA;
     if (v) {
         if (cudaMemset(c->d_status, 0, sizeof v) != cudaSuccess) return TRI_ATTN_ECUDA;
-        return TRI_ATTN_ETIMEOUT;
+        return (v & kStatusTimeoutMask) ? TRI_ATTN_ETIMEOUT : TRI_ATTN_ERANGE;
     }
     return TRI_ATTN_OK;
 }

@@ -29,6 +29,8 @@ enum : uint32_t {
     kStatusTimeoutMma = 1u << 1,
     kStatusTimeoutSoftmax = 1u << 2,
     kStatusTimeoutEpilogue = 1u << 3,
+    kStatusTimeoutMask = 0xFu,
+    kStatusRange = 1u << 4,          // a non-finite value from an f16 intermediate out of range
 };
 
 // Byte offsets of the workspace regions for one (config, I).  Every region

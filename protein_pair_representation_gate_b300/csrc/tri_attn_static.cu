@@ -11,9 +11,16 @@
 // The scratch array below is part of the module: every GPU on which the
 // library's module is loaded holds it (kStaticScratchBytes, 34.3 MB)
 // until the process exits.  Host code cannot use the array's name as a device
-// address (it names a host-side stand-in), so the device address is obtained
-// once per device with cudaGetSymbolAddress, with that device current, and
-// cached.
+// address (it names a host-side stand-in), so the device address is looked up
+// with cudaGetSymbolAddress, with the device current, and cached.  A device
+// address belongs to one CUDA context (the module is loaded per context), so
+// the cache is keyed by the context's process-unique id: a call made under
+// another context, or after cudaDeviceReset re-created the primary context,
+// looks the address up again instead of reusing a stale one.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
 #include <mutex>
 
 #include "tri_attn_internal.h"
@@ -29,22 +36,72 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct Cached {
+    unsigned long long ctx_id = 0;   // 0: nothing cached (context ids start at 1)
+    void* addr = nullptr;
+};
+Cached g_cache[kMaxDevices];
+std::atomic<int> g_inject{0};        // one-shot test hook (tri_attn_static_debug_inject)
 
-// Device address of the scratch array on the current device (set up on first use).
+// The driver's current-context queries, looked up once (no libcuda link needed).
+struct CtxFns {
+    PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+    static const CtxFns f = [] {
+        CtxFns r;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            r.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            r.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        return r;
+    }();
+    return f;
+}
+
+// Id of the context current on this thread (0 if it cannot be determined).
+unsigned long long current_ctx_id() {
+    const CtxFns& f = ctx_fns();
+    if (!f.get_current || !f.get_id) return 0;
+    CUcontext c = nullptr;
+    if (f.get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    if (f.get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current context (looked up on
+// the first call in each context).  Called after a runtime call has made the
+// device's context current.
 cudaError_t scratch_address(int dev, void** out) {
+    const unsigned long long id = current_ctx_id();
+    if (id == 0) return cudaErrorDeviceUninitialized;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    Cached& c = g_cache[dev];
+    if (c.ctx_id != id) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        c.addr = p;
+        c.ctx_id = id;
     }
-    *out = g_scratch_addr[dev];
+    *out = c.addr;
     return cudaSuccess;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    return pa < pb + nb && pb < pa + na;
+}
 
 }  // namespace
 }  // namespace tri_attn
@@ -66,11 +123,8 @@ extern "C" tri_attn_status tri_attn_forward_static(int node, int I, const void* 
     for (const void* p : wp)
         if (p && !aligned16(p)) return TRI_ATTN_EINVAL;
     const size_t pair_bytes = (size_t)I * I * 128 * 2;
-    {
-        const char* a = static_cast<const char*>(out);
-        const char* b = static_cast<const char*>(Z);
-        if (a < b + pair_bytes && b < a + pair_bytes) return TRI_ATTN_EINVAL;
-    }
+    if (overlaps(out, pair_bytes, Z, pair_bytes)) return TRI_ATTN_EINVAL;
+    if (token_mask && overlaps(token_mask, (size_t)I, out, pair_bytes)) return TRI_ATTN_EINVAL;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TRI_ATTN_ECUDA;
@@ -87,7 +141,9 @@ extern "C" tri_attn_status tri_attn_forward_static(int node, int I, const void* 
     if (scratch_address(dev, &base) != cudaSuccess) return TRI_ATTN_ECUDA;
     char* ws = static_cast<char*>(base);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + kStaticWorkspace);
-    if (!(reinterpret_cast<const char*>(out) + pair_bytes <= ws || ws + kStaticScratchBytes <= static_cast<const char*>(out)))
+    // no input or output may lie in the library's array
+    if (overlaps(out, pair_bytes, ws, kStaticScratchBytes) || overlaps(Z, pair_bytes, ws, kStaticScratchBytes) ||
+        (token_mask && overlaps(token_mask, (size_t)I, ws, kStaticScratchBytes)))
         return TRI_ATTN_EINVAL;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -110,5 +166,27 @@ extern "C" tri_attn_status tri_attn_forward_static(int node, int I, const void* 
     a.out = out;
     a.key_chunks = 1;
     a.status = status;
+    a.inject = g_inject.exchange(0);
     return sm103_forward(a, s, nullptr) == cudaSuccess ? TRI_ATTN_OK : TRI_ATTN_ECUDA;
+}
+
+extern "C" tri_attn_status tri_attn_static_status(void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TRI_ATTN_ECUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TRI_ATTN_EUNSUPPORTED;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TRI_ATTN_ECUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_static_scratch, sizeof v, kStaticWorkspace, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TRI_ATTN_ECUDA;
+    if (v == 0) return TRI_ATTN_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_static_scratch, &zero, sizeof zero, kStaticWorkspace, cudaMemcpyHostToDevice) != cudaSuccess)
+        return TRI_ATTN_ECUDA;
+    return (v & kStatusTimeoutMask) ? TRI_ATTN_ETIMEOUT : TRI_ATTN_ERANGE;
+}
+
+extern "C" tri_attn_status tri_attn_static_debug_inject(int fault) {
+    if (fault != TRI_ATTN_FAULT_NONE && fault != TRI_ATTN_FAULT_SKIP_STAGE) return TRI_ATTN_EINVAL;
+    g_inject.store(fault);
+    return TRI_ATTN_OK;
 }

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert pkg.status_string(s) and pkg.status_string(s) != "unknown status"
     assert pkg.status_string(99) == "unknown status"
 

@@ -133,3 +133,27 @@ def test_forward_ex_aliasing_rules(setup):
     assert torch.equal(Z, before)
     assert ctx.forward_status(0, 64, Z, t["mask"], t, ws, Z, None, nb, residual=True) == B.OK
     assert ctx.status_sync() == B.OK
+
+
+def test_large_layernorm_scale_is_finite_or_reported(setup):
+    """Intermediates of the sm103 path are f16 (|x| < 65504).  LayerNorm weights
+    far beyond a trained model's scale must give either finite output with an OK
+    status or the ERANGE status, never silent NaN: gamma = 50 stays inside the
+    f16 range (scores then form a hard argmax, so no oracle tolerance applies);
+    gamma = 1e5 pushes q, k, v and the pair bias past it."""
+    torch, t, ctx, ws = setup
+    for scale, want in ((50.0, B.OK), (1e5, B.ERANGE)):
+        w = dict(t)
+        w["ln_gamma"] = t["ln_gamma"] * scale
+        for node in ("start", "end"):
+            out = torch.full_like(t["Z"], float("nan"))
+            ctx.forward(node, 64, t["Z"], None, w, ws, out)
+            st = ctx.status_sync()
+            assert st == want, (scale, node, B.status_string(st))
+            if st == B.OK:
+                assert bool(torch.isfinite(out.float()).all()), (scale, node)
+    # the context is usable again at the normal scale
+    out = torch.empty_like(t["Z"])
+    ctx.forward("start", 64, t["Z"], None, t, ws, out)
+    assert ctx.status_sync() == B.OK
+    assert bool(torch.isfinite(out.float()).all())
