@@ -50,21 +50,31 @@ def parse():
 
 
 # DRAM traffic of one sm103_attention launch, from one ncu capture of dram__bytes_read.sum +
-# dram__bytes_write.sum at I=512 (start node: 270.7 MB read + 48.2 MB written; summary in
-# profiles/dram_traffic_complex_2048_I512.md), scaled to I=2048 by the pair count (x16): the kernel's
-# operand traffic (q, k, vT, g, bias, out) grows with I^2.  Valid only for the kernel sources it was
-# captured with (hash below); any change to them reports null until the capture is repeated.
-ATTN_TRAFFIC_I512 = 270.7e6 + 48.2e6
-ATTN_TRAFFIC_SRC = "866150c63524a8d0"
+# dram__bytes_write.sum at I=512 (start node; summary in profiles/dram_traffic_complex_2048_I512.md),
+# scaled to I=2048 by the pair count (x16): the kernel's operand traffic (q, k, vT, g, bias, out) grows
+# with I^2 (the per-line K / V re-reads of the line's other query tiles are L2 hits).  Valid only for
+# the attention kernel's sources it was captured with: the hash covers that kernel's section of
+# sm103_kernels.cu and the PTX helpers; any change to them reports null until the capture is repeated.
+ATTN_TRAFFIC_I512 = 270.816512e6 + 48.226048e6
+ATTN_TRAFFIC_SRC = "b538c90bd82cdd9c"
+
+
+def attention_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "protein_pair_representation_gate_b300", "csrc")
+    with open(os.path.join(csrc, "sm103_kernels.cu")) as fh:
+        text = fh.read()
+    a = text.index("namespace k2 {")
+    b = text.index("// Host side")
+    h.update(text[a:b].encode())
+    with open(os.path.join(csrc, "sm103_ptx.cuh"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def attention_traffic(I: int):
-    import hashlib
-    h = hashlib.sha256()
-    for f in ("sm103_kernels.cu", "sm103_ptx.cuh"):
-        with open(os.path.join(ROOT, "protein_pair_representation_gate_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != ATTN_TRAFFIC_SRC:
+    if ATTN_TRAFFIC_I512 is None or attention_source_hash() != ATTN_TRAFFIC_SRC:
         return None
     return ATTN_TRAFFIC_I512 * (I / 512) ** 2
 
