@@ -341,6 +341,56 @@ def secondary_runs(pkg, dev, peak):
                     "kernels_ms_per_forward": {k: sum(v) / (iters * len(nodes)) for k, v in kms.items()}})
         del t, op, out, pm
         torch.cuda.empty_cache()
+    res.extend(msa_runs(pkg, dev, peak))
+    return res
+
+
+def msa_runs(pkg, dev, peak):
+    """MSA row attention with pair bias at the Evoformer MSA shape (S = 512 rows,
+    I = 256 residues, c_m = 256, 8 heads of 32): the tensor-core path and, for
+    comparison, the CUDA-core path; CUDA events around the library call."""
+    import torch
+    from synth import make_msa_inputs
+    from synth.device import msa_inputs_to_device
+
+    inp = make_msa_inputs("msa_evoformer_512")
+    wl = inp.workload
+    t = msa_inputs_to_device(inp, dev)
+    out = torch.empty_like(t["Ms"])
+    stream = torch.cuda.current_stream(dev)
+    res = []
+    for force_simt, iters in ((False, 10), (True, 2)):
+        op = pkg.MSARowAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, force_simt=force_simt)
+
+        def one():
+            op(t["Ms"], t["Z"], t, msa_mask=t["msa_mask"], out=out, stream=stream)
+
+        for _ in range(2):
+            one()
+        op.ctx.set_timing(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        kms = {}
+        for kname, ms in op.ctx.kernel_times():
+            kms.setdefault(kname, []).append(ms)
+        op.ctx.set_timing(False)
+        st = op.ctx.status_sync(stream)
+        if st != 0:
+            raise RuntimeError(f"msa_evoformer_512: {pkg.status_string(st)}")
+        ms_fwd = e0.elapsed_time(e1) / iters
+        tf = wl.attention_flops() / (ms_fwd * 1e-3) / 1e12
+        res.append({"workload": wl.name, "S": wl.S, "I": wl.I, "c_m": wl.c_m,
+                    "path": "sm103" if op.path(wl.c_m) == pkg.PATH_SM103 else "simt",
+                    "ms_per_forward": ms_fwd, "tflops": tf, "frac_of_peak": tf / peak,
+                    "kernels_ms_per_forward": {k: sum(v) / iters for k, v in kms.items()}})
+        del op
+    del t, out
+    torch.cuda.empty_cache()
     return res
 
 

@@ -191,8 +191,14 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* ctx, int node, int I,
  * the pair mask of tri_attn_forward_ex does.
  *
  * The context supplies c_z (pair channels), heads, head_dim, dtype, ln_eps and
- * key_chunks; it runs on the CUDA-core kernels (any context path; head_dim 8,
- * 16, 32 or 64), fp32 arithmetic on dtype storage. */
+ * key_chunks.  Two paths (tri_attn_msa_path):
+ *   sm103  bf16, c_m = 256, c_z = 128, 8 heads of 32 (the Evoformer's MSA row
+ *          attention), on an sm_103 device without force_simt: the MSA and pair
+ *          projections on tcgen05 tensor cores with f16 intermediates (q, k, v,
+ *          gate, pair bias, gated output u) and fp32 accumulation; the attention
+ *          kernel of tri_attn_forward; ERANGE as there.
+ *   SIMT   any other supported shape (head_dim 8, 16, 32 or 64): CUDA-core
+ *          kernels, fp32 arithmetic on dtype storage. */
 typedef struct {
     const float* ln_m_gamma;  /* [c_m] fp32                   */
     const float* ln_m_beta;   /* [c_m] fp32                   */
@@ -208,9 +214,13 @@ typedef struct {
     const void*  w_b;         /* [c_z, H] dtype               */
 } tri_attn_msa_weights;
 
+/* Path (tri_attn_path_kind) tri_attn_msa_forward takes on this context for
+ * c_m MSA channels, or -1 for a NULL context. */
+int tri_attn_msa_path(const tri_attn_ctx* ctx, int c_m);
+
 /* Bytes of device workspace tri_attn_msa_forward needs for S rows of I
- * residues (0 for a NULL context, S outside 1..16384 or I outside 1..I_max).
- * Same ownership rules as tri_attn_workspace_bytes. */
+ * residues, whichever path it takes (0 for a NULL context, S outside 1..16384
+ * or I outside 1..I_max).  Same ownership rules as tri_attn_workspace_bytes. */
 size_t tri_attn_msa_workspace_bytes(const tri_attn_ctx* ctx, int S, int I);
 
 /*   S           MSA rows, 1 <= S <= 16384

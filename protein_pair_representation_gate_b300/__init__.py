@@ -63,9 +63,13 @@ class MSARowAttention:
     """
 
     def __init__(self, c_z: int, heads: int, head_dim: int, I_max: int, dtype: str = "bf16",
-                 key_chunks: int = 1, ln_eps: float = 1e-5):
-        self.ctx = TriAttn(TriAttnConfig(c_z, heads, head_dim, I_max, dtype, ln_eps, key_chunks, True))
+                 key_chunks: int = 1, ln_eps: float = 1e-5, force_simt: bool = False):
+        self.ctx = TriAttn(TriAttnConfig(c_z, heads, head_dim, I_max, dtype, ln_eps, key_chunks, force_simt))
         self._ws = None
+
+    def path(self, c_m: int) -> int:
+        """PATH_SM103 or PATH_SIMT: the kernels a forward with c_m MSA channels runs."""
+        return self.ctx.msa_path(c_m)
 
     def workspace(self, S: int, I: int, device):
         import torch

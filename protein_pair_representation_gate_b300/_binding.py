@@ -23,7 +23,7 @@ EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_wor
            "tri_attn_forward", "tri_attn_status_sync", "tri_attn_set_timing", "tri_attn_kernel_times",
            "tri_attn_status_string", "tri_attn_forward_static", "tri_attn_debug_inject", "tri_attn_forward_ex",
            "tri_attn_msa_workspace_bytes", "tri_attn_msa_forward", "tri_attn_static_status",
-           "tri_attn_static_debug_inject")
+           "tri_attn_static_debug_inject", "tri_attn_msa_path")
 FAULT_NONE, FAULT_SKIP_STAGE = 0, 1
 
 
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tri_attn_forward_ex.argtypes = [vp, i, i, vp, vp, ctypes.POINTER(Options), ctypes.POINTER(Weights), vp, sz,
                                         vp, vp]
     lib.tri_attn_forward_ex.restype = i
+    lib.tri_attn_msa_path.argtypes = [vp, i]
+    lib.tri_attn_msa_path.restype = i
     lib.tri_attn_msa_workspace_bytes.argtypes = [vp, i, i]
     lib.tri_attn_msa_workspace_bytes.restype = sz
     lib.tri_attn_msa_forward.argtypes = [vp, i, i, i, vp, vp, vp, ctypes.POINTER(MsaWeights), i, vp, sz, vp, vp]
@@ -215,6 +217,9 @@ class TriAttn:
         return self.lib.tri_attn_forward_ex(self._h, NODES.get(node, node), I, _ptr(Z), _ptr(mask), ctypes.byref(opt),
                                             ctypes.byref(w), _ptr(workspace), workspace_bytes, _ptr(out),
                                             _stream_ptr(stream))
+
+    def msa_path(self, c_m: int) -> int:
+        return self.lib.tri_attn_msa_path(self._h, c_m)
 
     def msa_workspace_bytes(self, S: int, I: int) -> int:
         return int(self.lib.tri_attn_msa_workspace_bytes(self._h, S, I))

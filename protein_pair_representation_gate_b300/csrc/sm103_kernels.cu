@@ -418,6 +418,8 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
 // =====================================================================================
 struct AttnParams {
     int node, I, I_pad, nk, k_begin, k_end, first, last;
+    int h0;                    // MSA build: first of the 4 heads of this launch (of 8); 0 otherwise
+    __half* u;                 // MSA build: gated outputs [lines][I_pad][8 x 32] (f16), written per head
     int inject;                // test hook: block (0,0) skips the load of stage 1
     const uint8_t* mask;
     const uint8_t* pmask;      // [I, I] pair mask over the pairs of Z, or NULL
@@ -434,10 +436,10 @@ struct AttnParams {
 // set when key w*64 + kk < I and the pair mask admits it on that line (starting
 // node: M[L, key]; ending node: M[key, L]).  One extra zero word per line lets a
 // key tile that starts off a 64-key boundary (key chunks) read two words.
-__global__ void __launch_bounds__(128) sm103_pair_keybits(const uint8_t* pm, int node, int I, int words,
+__global__ void __launch_bounds__(128) sm103_pair_keybits(const uint8_t* pm, int node, int I, int lines, int words,
                                                           uint64_t* kbits) {
     const int idx = blockIdx.x * 128 + threadIdx.x;
-    if (idx >= I * words) return;
+    if (idx >= lines * words) return;
     const int L = idx / words, w = idx % words;
     uint64_t bits = 0;
     for (int kk = 0; kk < 64; ++kk) {
@@ -492,13 +494,22 @@ __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  /
 static_assert(kBias % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 }  // namespace k2
 
-template <bool kEx>
+// kMsa: the build for MSA row attention (always with kEx): a line is an MSA row,
+// the launch covers heads h0 .. h0+3 of 8 (q, k, v^T, g and the pair bias hold 8
+// heads per line), the MSA mask arrives as the pair mask's key bits, and each
+// head's gated output goes to global memory for the separate output projection
+// (no W_o, no epilogue here).
+template <bool kEx, bool kMsa>
 __global__ void __launch_bounds__(k2::kThreads, 1)
 sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapWo, AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     using LY = k2::Lay<kEx>;
+    static_assert(kEx || !kMsa, "the MSA build is a pair-mask build");
+    constexpr int NHT = kMsa ? 8 : NH;         // heads stored per line
+    const int h0 = kMsa ? p.h0 : 0;
+    const bool fused_out = !kMsa && p.last;   // output projection and store in this kernel
     if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     const int L = blockIdx.y;
     const int xq0 = blockIdx.x * 256;
@@ -624,14 +635,14 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
         bool ok = true;
         int it_issued = 0, skipped = -1, q_loads = 0;   // for the drain on the abort path
-        if (leader && p.last) {                   // W_o^T for the output projection at the block end
+        if (leader && fused_out) {                // W_o^T for the output projection at the block end
             prefetch_tmap(&mapWo);
             mbar_arrive_expect_tx(w_full, 32768);
             tma_load_2d(sm + LY::kWo, &mapWo, w_full, 0, 0);
             tma_load_2d(sm + LY::kWo + 16384, &mapWo, w_full, 64, 0);
         }
         for (int h = 0, it = 0; ok && h < NH; ++h) {
-            const int lh = L * NH + h;
+            const int lh = L * NHT + h0 + h;
             for (int t = 0; t < nk; ++t, ++it) {
                 const int st = it % k2::kStages;
                 if (t == 0) {
@@ -676,7 +687,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 __syncwarp();
             }
         }
-        if (p.last) {
+        if (fused_out) {
             // the block must not end with the W_o^T copy still writing its shared
             // memory, even when another role gave up (bounded, ignores the abort flag)
             volatile int keep_waiting = 0;
@@ -806,7 +817,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (nx < NT && ++tn == nk) { tn = 0; ++hn; }
             if (++tp == nk) tp = 0;
         }
-        if (ok && p.last) {                           // output projection: out = u W_o
+        if (ok && fused_out) {                        // output projection: out = u W_o
             constexpr uint32_t idP = idesc_f16_f32(128, 128);
             ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, abort) && mbar_wait(u_full + g, 0, abort));
             if (ok && leader) {
@@ -843,7 +854,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     const int h = j / nk, t = j - h * nk;
                     mbar_arrive_expect_tx(b_full + bs, k2::kBiasBytes);
                     tma_load_2d(sm + k2::kBias + bs * k2::kBiasBytes, &mapB, b_full + bs, p.k_begin + t * k2::kKT,
-                                h * p.I_pad + xq0 + g * 128);
+                                (h0 + h) * p.I_pad + xq0 + g * 128);
                 }
                 __syncwarp();
                 if (g) ++nb1; else ++nb0;
@@ -886,7 +897,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         // global-memory latency is hidden (heads of one tile load it in finalize)
         uint4 gpre[4];
         auto load_gate = [&](int hh) {
-            const uint4* gp = reinterpret_cast<const uint4*>(p.g + (((size_t)L * NH + hh) * p.I_pad + x) * HD);
+            const uint4* gp = reinterpret_cast<const uint4*>(p.g + (((size_t)L * NHT + h0 + hh) * p.I_pad + x) * HD);
 #pragma unroll
             for (int i = 0; i < 4; ++i) gpre[i] = gp[i];
         };
@@ -908,7 +919,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 chk += fabsf(o[e]);
             }
             if (x < p.I && !(chk < INFINITY)) atomicOr(p.status, kStatusRange);
-            const size_t srow = ((size_t)(L * NH + hp)) * p.I_pad + x;
+            const size_t srow = ((size_t)(L * NHT + h0 + hp)) * p.I_pad + x;
             if (!p.first) {
                 const float lr = p.lse_run[srow];
                 const float top = fmaxf(lr, lse);
@@ -946,7 +957,13 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         u[4 * i + jj] = pack_f16(f16lo(gw[jj]) * o[e], f16hi(gw[jj]) * o[e + 1]);
                     }
                 }
-                tmem_st16(tU + hp * 16, u);
+                if constexpr (kMsa) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.u + ((size_t)L * p.I_pad + x) * (NHT * HD) + (h0 + hp) * HD);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
+                } else {
+                    tmem_st16(tU + hp * 16, u);
+                }
             }
         };
 
@@ -1052,7 +1069,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             finalize(NH - 1);
         }
         if (!ok) set_abort(abort, p.status, kStatusTimeoutSoftmax);
-        if (ok && p.last) {
+        if (ok && fused_out) {
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -1194,10 +1211,13 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     if (!(attr_set.load(std::memory_order_acquire) & dev_bit)) {
         cudaError_t e = cudaFuncSetAttribute(sm103_ln_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::kSmem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sm103_attention<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(sm103_attention<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  k2::Lay<false>::kSmem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sm103_attention<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(sm103_attention<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 k2::Lay<true>::kSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(sm103_attention<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  k2::Lay<true>::kSmem);
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(dev_bit, std::memory_order_release);
@@ -1268,7 +1288,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         kbits = reinterpret_cast<uint64_t*>(a.ws + W.kbits);
         const int words = Ip / 64 + 1;
         if (tm) tm->begin("sm103_pair_keybits", s);
-        sm103_pair_keybits<<<(I * words + 127) / 128, 128, 0, s>>>(a.pair_mask, a.node, I, words, kbits);
+        sm103_pair_keybits<<<(I * words + 127) / 128, 128, 0, s>>>(a.pair_mask, a.node, I, I, words, kbits);
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1296,15 +1316,98 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.out = static_cast<__nv_bfloat16*>(a.out);
         ap.status = a.status;
         ap.inject = k0 == 0 ? a.inject : 0;
+        ap.h0 = 0;
+        ap.u = nullptr;
         dim3 grid(Ip / 256, I);
         if (tm) tm->begin("sm103_attention", s);
         if (ap.kbits != nullptr || ap.Z != nullptr)
-            sm103_attention<true><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+            sm103_attention<true, false><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
         else
-            sm103_attention<false><<<grid, k2::kThreads, k2::Lay<false>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+            sm103_attention<false, false><<<grid, k2::kThreads, k2::Lay<false>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+                 uint32_t box_rows, int swizzle_bytes, bool bf16) {
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return map2d(m, base, cols, rows, row_bytes, box_cols, box_rows, sw,
+                 bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+bool sm103_map3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    return map3d(m, base, d0, d1, d2, s1, s2, b0, b1, b2);
+}
+
+// MSA row attention on the attention kernel's MSA build: per key chunk, two
+// launches (heads 0-3 and 4-7) over S lines.
+cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTimer* tm) {
+    static std::atomic<uint64_t> attr_set{0};
+    const int dev = current_device();
+    const uint64_t dev_bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (!(attr_set.load(std::memory_order_acquire) & dev_bit)) {
+        cudaError_t e = cudaFuncSetAttribute(sm103_attention<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             k2::Lay<true>::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(dev_bit, std::memory_order_release);
+    }
+    const int Ip = m.I_pad;
+    const uint64_t rows_qk = (uint64_t)m.S * 8 * Ip;
+    CUtensorMap mQ, mK, mV, mB;
+    if (!map2d(&mQ, m.q, HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mK, m.k, HD, rows_qk, HD * 2, HD, k2::kKT, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mV, m.vt, Ip, (uint64_t)m.S * 8 * HD, (uint64_t)Ip * 2, 64, HD, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&mB, m.bias, Ip, (uint64_t)8 * Ip, (uint64_t)Ip * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e;
+    uint64_t* kbits = nullptr;
+    if (m.msa_mask != nullptr) {
+        kbits = m.kbits;
+        const int words = Ip / 64 + 1;
+        if (tm) tm->begin("sm103_pair_keybits", s);
+        sm103_pair_keybits<<<(m.S * words + 127) / 128, 128, 0, s>>>(m.msa_mask, TRI_ATTN_STARTING, m.I, m.S, words,
+                                                                    kbits);
+        if (tm) tm->end(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const int cs = chunk_size(m.I, m.key_chunks);
+    for (int k0 = 0; k0 < m.I; k0 += cs) {
+        const int k1e = k0 + cs < m.I ? k0 + cs : m.I;
+        for (int h0 = 0; h0 < 8; h0 += NH) {
+            AttnParams ap{};
+            ap.node = TRI_ATTN_STARTING;
+            ap.I = m.I;
+            ap.I_pad = Ip;
+            ap.k_begin = k0;
+            ap.k_end = k1e;
+            ap.nk = (k1e - k0 + k2::kKT - 1) / k2::kKT;
+            ap.first = k0 == 0;
+            ap.last = k1e == m.I;
+            ap.h0 = h0;
+            ap.u = m.u;
+            ap.mask = nullptr;
+            ap.pmask = m.msa_mask;
+            ap.kbits = kbits;
+            ap.Z = nullptr;
+            ap.g = m.g;
+            ap.bo = nullptr;
+            ap.o_run = m.o_run;
+            ap.lse_run = m.lse_run;
+            ap.out = nullptr;
+            ap.status = m.status;
+            ap.inject = 0;
+            dim3 grid(Ip / 256, m.S);
+            if (tm) tm->begin("sm103_attention", s);
+            sm103_attention<true, true><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mB, ap);
+            if (tm) tm->end(s);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

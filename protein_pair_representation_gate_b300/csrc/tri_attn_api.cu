@@ -14,6 +14,7 @@ struct tri_attn_ctx {
     tri_attn_config cfg;
     int device = 0;
     int path = TRI_ATTN_PATH_SIMT;
+    bool msa_sm103 = false;  // MSA forwards with c_m = 256 take the sm103 path
     uint32_t* d_status = nullptr;
 
     // timing
@@ -97,18 +98,19 @@ tri_attn_status tri_attn_create(const tri_attn_config* cfg, tri_attn_ctx** out) 
     if (!sm103 && d != 8 && d != 16 && d != 32 && d != 64) return TRI_ATTN_EUNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TRI_ATTN_ECUDA;
-    if (sm103) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return TRI_ATTN_ECUDA;
-        if (major != 10 || minor != 3) return TRI_ATTN_EUNSUPPORTED;   // kernels are built for sm_103a only
-    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return TRI_ATTN_ECUDA;
+    const bool is_sm103 = major == 10 && minor == 3;                  // kernels are built for sm_103a only
+    if (sm103 && !is_sm103) return TRI_ATTN_EUNSUPPORTED;
     tri_attn_ctx* c = new (std::nothrow) tri_attn_ctx();
     if (!c) return TRI_ATTN_ENOMEM;
     c->cfg = *cfg;
     c->device = dev;
     c->path = sm103 ? TRI_ATTN_PATH_SM103 : TRI_ATTN_PATH_SIMT;
+    c->msa_sm103 = is_sm103 && !cfg->force_simt &&
+                   sm103_msa_supported(kMsaCm, cfg->c_z, cfg->heads, cfg->head_dim, cfg->dtype);
     if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(c->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
         cudaFree(c->d_status);
@@ -201,9 +203,19 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* c, int node, int I, const void
     return TRI_ATTN_OK;
 }
 
+int tri_attn_msa_path(const tri_attn_ctx* c, int c_m) {
+    if (!c) return -1;
+    const tri_attn_config& g = c->cfg;
+    return c->msa_sm103 && sm103_msa_supported(c_m, g.c_z, g.heads, g.head_dim, g.dtype) ? TRI_ATTN_PATH_SM103
+                                                                                       : TRI_ATTN_PATH_SIMT;
+}
+
 size_t tri_attn_msa_workspace_bytes(const tri_attn_ctx* c, int S, int I) {
     if (!c || S < 1 || S > kMsaMaxRows || I < 1 || I > c->cfg.I_max) return 0;
-    return simt_msa_layout(S, I, c->cfg.heads, c->cfg.head_dim, c->cfg.key_chunks).total;
+    // enough for either path (the path also depends on c_m, which this call does not take)
+    const size_t simt = simt_msa_layout(S, I, c->cfg.heads, c->cfg.head_dim, c->cfg.key_chunks).total;
+    const size_t sm103 = c->msa_sm103 ? sm103_msa_layout(S, I, c->cfg.key_chunks).total : 0;
+    return simt > sm103 ? simt : sm103;
 }
 
 tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, const void* msa, const uint8_t* msa_mask,
@@ -221,7 +233,9 @@ tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, con
                         w->ln_z_gamma, w->ln_z_beta, w->w_b};
     for (const void* p : wp)
         if (p && !aligned(p, 16)) return TRI_ATTN_EINVAL;
-    const Workspace lay = simt_msa_layout(S, I, g.heads, g.head_dim, g.key_chunks);
+    const bool on_sm103 = tri_attn_msa_path(c, c_m) == TRI_ATTN_PATH_SM103;
+    const Workspace lay = on_sm103 ? sm103_msa_layout(S, I, g.key_chunks)
+                                   : simt_msa_layout(S, I, g.heads, g.head_dim, g.key_chunks);
     if (workspace_bytes < lay.total) return TRI_ATTN_ENOMEM;
     const size_t esz = g.dtype == TRI_ATTN_F32 ? 4 : 2;
     const size_t msa_bytes = (size_t)S * I * c_m * esz, z_bytes = (size_t)I * I * g.c_z * esz;
@@ -252,9 +266,10 @@ tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, con
     a.ws = static_cast<char*>(workspace);
     a.lay = &lay;
     a.out = out;
+    a.status = c->d_status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LaunchTimer* t = c->timing ? &c->timer : nullptr;
-    const cudaError_t e = simt_msa_forward(a, g.dtype, s, t);
+    const cudaError_t e = on_sm103 ? sm103_msa_forward(a, s, t) : simt_msa_forward(a, g.dtype, s, t);
     if (e != cudaSuccess) {
         fprintf(stderr, "tri_attn_msa_forward: %s\n", cudaGetErrorString(e));
         return TRI_ATTN_ECUDA;

@@ -12,6 +12,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tri_attn.h"
@@ -87,6 +89,7 @@ struct MsaArgs {
     char* ws;
     const Workspace* lay;
     void* out;                     // [S, I, c_m]
+    uint32_t* status = nullptr;    // device status word (sm103 path)
 };
 constexpr int kMsaMaxRows = 16384;
 Workspace simt_msa_layout(int S, int I, int H, int d, int key_chunks);
@@ -125,6 +128,54 @@ constexpr Workspace sm103_layout(int I, int key_chunks) {
     return w;
 }
 cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* t);
+
+// MSA row attention on the sm103 path: bf16, c_m = 256, c_z = 128, 8 heads of 32.
+constexpr int kMsaCm = 256, kMsaHeads = 8;
+bool sm103_msa_supported(int c_m, int c_z, int H, int d, int dtype);
+
+// Workspace of the sm103 MSA path (tokens padded to a multiple of 256).
+constexpr Workspace sm103_msa_layout(int S, int I, int key_chunks) {
+    Workspace w;
+    w.I = I;
+    w.I_pad = round_up(I, 256);
+    const size_t P = (size_t)S * w.I_pad;            // (MSA row, residue) slots
+    size_t off = 0;
+    auto take = [&off](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    w.wprep = take((size_t)1024 * 256 * 2);           // (gamma_m . W)^T for q | k | v | g, bf16
+    w.cst = take((size_t)512 * 4 * 4);                // per column pair {colsum x2, offset x2}
+    w.wb32 = take((size_t)128 * 8 * 4 + 2 * 8 * 4);   // gamma_z . W_b, its column sums, beta_z W_b
+    w.wo_t = take((size_t)256 * 256 * 2);             // W_o^T, f16
+    w.bo = take(256 * 4);
+    w.kbits = take((size_t)S * (w.I_pad / 64 + 1) * 8);
+    w.q = take(P * 256 * 2);
+    w.k = take(P * 256 * 2);
+    w.v = take(P * 256 * 2);
+    w.g = take(P * 256 * 2);
+    w.u = take(P * 256 * 2);
+    w.bias = take((size_t)8 * w.I_pad * w.I_pad * 2);
+    if (key_chunks > 1) {
+        w.o_run = take(P * 256 * 4);
+        w.lse_run = take(P * 8 * 4);
+    }
+    w.total = off;
+    return w;
+}
+cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* t);
+
+// Pieces of the sm103 triangle kernels the MSA path shares.
+struct MsaAttnArgs {
+    int S, I, I_pad, key_chunks;
+    __half *q, *k, *vt, *g, *bias, *u;
+    float *o_run, *lse_run;
+    const uint8_t* msa_mask;
+    uint64_t* kbits;
+    uint32_t* status;
+};
+cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTimer* t);
+bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+                 uint32_t box_rows, int swizzle_bytes, bool bf16);
+bool sm103_map3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
 
 // Chunk bounds shared by both paths: size = round_up(ceil(I / n), 8).
 inline int chunk_size(int I, int n) {

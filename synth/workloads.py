@@ -322,3 +322,31 @@ def make_msa_inputs(wl: MsaWorkload | str, S: int | None = None, I: int | None =
         b_g=np.ones(C, dtype=np.float32),
         b_o=np.zeros(cm, dtype=np.float32),
     )
+
+
+# ---------------------------------------------------------------- affine parameters
+# The default workloads keep LayerNorm gamma = 1, beta = 0, gate bias 1 and output
+# bias 0.  with_affine_params swaps in seeded non-trivial values so that a test
+# sees every term those parameters enter: gamma ~ 1 + 0.25 N(0, 1), beta, gate
+# bias and output bias ~ 0.25 N(0, 1), each from its own stream (20 + its index
+# in AFFINE_FIELDS).
+AFFINE_FIELDS = ("ln_gamma", "ln_beta", "b_g", "b_o", "ln_m_gamma", "ln_m_beta", "ln_z_gamma", "ln_z_beta")
+STREAM_AFFINE = 20
+
+
+def with_affine_params(inp):
+    """A copy of `inp` (Inputs or MsaInputs) with seeded non-trivial LayerNorm,
+    gate-bias and output-bias parameters (float32, like the defaults)."""
+    from dataclasses import fields, replace
+    names = {f.name for f in fields(inp)}
+    seed = inp.workload.seed
+    new = {}
+    for k, name in enumerate(AFFINE_FIELDS):
+        if name not in names:
+            continue
+        n = getattr(inp, name).shape[0]
+        x = 0.25 * normal(seed, STREAM_AFFINE + k, n)
+        if name.endswith("gamma"):
+            x = x + 1.0
+        new[name] = x.astype(np.float32)
+    return replace(inp, **new)

@@ -7,7 +7,7 @@ import functools
 import numpy as np
 
 from oracle import pair_bias, triangle_attention
-from synth import make_inputs
+from synth import make_inputs, with_affine_params
 
 # Tolerances: fp32 path max-abs 1e-4; bf16 inputs with fp32 accumulation
 # max-abs 2e-2 and relative L2 error 5e-3 over the compared outputs.
@@ -17,7 +17,7 @@ BF16_REL_L2 = 5e-3
 
 
 @functools.lru_cache(maxsize=4)
-def inputs(name: str, I: int | None = None, n_pad: int | None = None):
+def inputs(name: str, I: int | None = None, n_pad: int | None = None, affine: bool = False):
     from dataclasses import replace
     from synth.workloads import WORKLOADS
     wl = WORKLOADS[name]
@@ -25,28 +25,30 @@ def inputs(name: str, I: int | None = None, n_pad: int | None = None):
         wl = replace(wl, I=I, n_pad=min(wl.n_pad if n_pad is None else n_pad, I))
     elif n_pad is not None:
         wl = replace(wl, n_pad=n_pad)
-    return make_inputs(wl)
+    inp = make_inputs(wl)
+    return with_affine_params(inp) if affine else inp
 
 
 @functools.lru_cache(maxsize=2)
-def oracle_state(name, I=None, n_pad=None):
-    inp = inputs(name, I, n_pad)
+def oracle_state(name, I=None, n_pad=None, affine=False):
+    inp = inputs(name, I, n_pad, affine)
     a = inp.oracle_args()
     return a, pair_bias(a["Z"], a["ln_gamma"], a["ln_beta"], a["w_b"])
 
 
-def oracle_out(name, node, lines=None, I=None, n_pad=None, key_chunks=1):
-    a, bias = oracle_state(name, I, n_pad)
+def oracle_out(name, node, lines=None, I=None, n_pad=None, key_chunks=1, affine=False):
+    a, bias = oracle_state(name, I, n_pad, affine)
     return triangle_attention(node, a["Z"], a["mask"], a, lines=lines, key_chunks=key_chunks, bias=bias)
 
 
-def run_library(name, nodes=("start", "end"), I=None, n_pad=None, key_chunks=1, force_simt=False, repeat=1):
+def run_library(name, nodes=("start", "end"), I=None, n_pad=None, key_chunks=1, force_simt=False, repeat=1,
+                affine=False):
     """Outputs of tri_attn_forward (through the C-ABI) as float64 numpy arrays, per node."""
     import torch
     import protein_pair_representation_gate_b300 as pkg
     from synth.device import inputs_to_device
 
-    inp = inputs(name, I, n_pad)
+    inp = inputs(name, I, n_pad, affine)
     wl = inp.workload
     t = inputs_to_device(inp, "cuda")
     op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=key_chunks,

@@ -107,3 +107,17 @@ def test_simt_path_bf16_small():
     assert res["path"] == 0
     for node in NODES:
         assert_close(res[node], oracle_out("evoformer_256", node, I=80), "bf16", f"simt bf16 {node}")
+
+
+@pytest.mark.parametrize("force_simt", [False, True])
+def test_affine_params(force_simt):
+    """Non-trivial LayerNorm gamma / beta, gate bias and output bias: every term
+    they enter (the folded gamma, the beta offset, b_g, b_o) is exercised."""
+    res = run_library("evoformer_256", I=129, force_simt=force_simt, affine=True)
+    assert res["path"] == (0 if force_simt else 1)
+    for node in NODES:
+        want = oracle_out("evoformer_256", node, I=129, affine=True)
+        assert_close(res[node], want, "bf16", f"affine params {node} simt={force_simt}")
+    res_f32 = run_library("tiny_f32", affine=True)
+    for node in NODES:
+        assert_close(res_f32[node], oracle_out("tiny_f32", node, affine=True), "f32", f"affine f32 {node}")
