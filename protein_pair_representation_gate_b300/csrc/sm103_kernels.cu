@@ -418,7 +418,6 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
 // =====================================================================================
 struct AttnParams {
     int node, I, I_pad, nk, k_begin, k_end, first, last;
-    int h0;                    // MSA build: first of the 4 heads of this launch (of 8); 0 otherwise
     __half* u;                 // MSA build: gated outputs [lines][I_pad][8 x 32] (f16), written per head
     int inject;                // test hook: block (0,0) skips the load of stage 1
     const uint8_t* mask;
@@ -495,7 +494,7 @@ static_assert(kBias % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 10
 }  // namespace k2
 
 // kMsa: the build for MSA row attention (always with kEx): a line is an MSA row,
-// the launch covers heads h0 .. h0+3 of 8 (q, k, v^T, g and the pair bias hold 8
+// a block covers heads h0 = 4 blockIdx.z .. h0+3 of 8 (q, k, v^T, g and the pair bias hold 8
 // heads per line), the MSA mask arrives as the pair mask's key bits, and each
 // head's gated output goes to global memory for the separate output projection
 // (no W_o, no epilogue here).
@@ -508,7 +507,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     using LY = k2::Lay<kEx>;
     static_assert(kEx || !kMsa, "the MSA build is a pair-mask build");
     constexpr int NHT = kMsa ? 8 : NH;         // heads stored per line
-    const int h0 = kMsa ? p.h0 : 0;
+    const int h0 = kMsa ? static_cast<int>(blockIdx.z) * NH : 0;   // MSA build: heads h0 .. h0 + 3 of the row
     const bool fused_out = !kMsa && p.last;   // output projection and store in this kernel
     if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
     const int L = blockIdx.y;
@@ -1159,7 +1158,7 @@ bool map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint6
 }
 
 bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-           uint32_t b0, uint32_t b1, uint32_t b2) {
+           uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -1167,7 +1166,7 @@ bool map3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t 
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1316,7 +1315,6 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.out = static_cast<__nv_bfloat16*>(a.out);
         ap.status = a.status;
         ap.inject = k0 == 0 ? a.inject : 0;
-        ap.h0 = 0;
         ap.u = nullptr;
         dim3 grid(Ip / 256, I);
         if (tm) tm->begin("sm103_attention", s);
@@ -1341,12 +1339,13 @@ bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 }
 
 bool sm103_map3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
-    return map3d(m, base, d0, d1, d2, s1, s2, b0, b1, b2);
+                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes) {
+    return map3d(m, base, d0, d1, d2, s1, s2, b0, b1, b2,
+                 swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// MSA row attention on the attention kernel's MSA build: per key chunk, two
-// launches (heads 0-3 and 4-7) over S lines.
+// MSA row attention on the attention kernel's MSA build: per key chunk, one
+// launch over (query blocks, S lines, head halves 0-3 and 4-7).
 cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTimer* tm) {
     static std::atomic<uint64_t> attr_set{0};
     const int dev = current_device();
@@ -1379,7 +1378,7 @@ cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTime
     const int cs = chunk_size(m.I, m.key_chunks);
     for (int k0 = 0; k0 < m.I; k0 += cs) {
         const int k1e = k0 + cs < m.I ? k0 + cs : m.I;
-        for (int h0 = 0; h0 < 8; h0 += NH) {
+        {
             AttnParams ap{};
             ap.node = TRI_ATTN_STARTING;
             ap.I = m.I;
@@ -1389,7 +1388,6 @@ cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTime
             ap.nk = (k1e - k0 + k2::kKT - 1) / k2::kKT;
             ap.first = k0 == 0;
             ap.last = k1e == m.I;
-            ap.h0 = h0;
             ap.u = m.u;
             ap.mask = nullptr;
             ap.pmask = m.msa_mask;
@@ -1402,7 +1400,7 @@ cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTime
             ap.out = nullptr;
             ap.status = m.status;
             ap.inject = 0;
-            dim3 grid(Ip / 256, m.S);
+            dim3 grid(Ip / 256, m.S, 8 / NH);
             if (tm) tm->begin("sm103_attention", s);
             sm103_attention<true, true><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mB, ap);
             if (tm) tm->end(s);

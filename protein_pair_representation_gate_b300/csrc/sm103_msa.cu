@@ -12,24 +12,27 @@
 //                    projection GEMM then runs on the raw MSA rows:
 //                    LN(m) W = rstd * (m (gamma.W) - mu * colsum) + beta W),
 //                    the gamma_z-folded pair-bias weights, and W_o^T in f16.
-//   sm103_msa_bias   the pair bias of the 8 heads from Z (one warp per pair:
-//                    LayerNorm_z and 8 dot products of length 128), log2(e)
-//                    scaled, f16; padded keys get -30000 (finite, as on the
-//                    triangle path: 2^-30000 is 0 in fp32).
-//   sm103_msa_gemm<0>  persistent tcgen05 GEMM, one 128-column block of the
-//                    1024 projection columns per CTA (its 64 KB of weights
-//                    resident in shared memory), 128 MSA positions per tile,
-//                    K = 256 in 16 MMAs of K = 16 into a double-buffered TMEM
-//                    accumulator; the epilogue finishes the LayerNorm and writes
-//                    q (log2(e)/sqrt(d) folded in), k, v^T and the sigmoid gate
-//                    in the layouts of the attention kernel.
-//   sm103_attention (MSA build, in sm103_kernels.cu): two launches of four
-//                    heads over the S rows; the MSA mask excludes keys per row
-//                    through the pair-mask key bits; each head's gated output
-//                    u goes to global memory.
-//   sm103_msa_gemm<1>  the same GEMM for out = u W_o (f16 operands), the output
-//                    bias, the MSA mask (masked positions are 0, or Ms with the
-//                    residual) and the residual in the epilogue.
+//   sm103_msa_bias   the pair bias of the 8 heads from Z (LayerNorm_z and 8 dot
+//                    products of length 128 per pair, from a shared-memory copy
+//                    of 64 pairs), log2(e) scaled, f16; padded keys get -30000
+//                    (finite, as on the triangle path: 2^-30000 is 0 in fp32).
+//   sm103_msa_ln_stats  LayerNorm_m mean and 1/std of every (row, residue) slot.
+//   sm103_msa_gemm<0>  persistent tcgen05 GEMM, one 256-column group (q, k, v
+//                    or gate) per CTA with its 128 KB of weights resident in
+//                    shared memory, 128 MSA slots per tile, K = 256 in 16 MMAs of
+//                    128 x 256 x 16 plus one K-step for the LayerNorm terms into a
+//                    double-buffered TMEM accumulator; 8 epilogue warps scale by
+//                    the slot's 1/std and write q (log2(e)/sqrt(d) folded in), k,
+//                    v^T and the sigmoid gate in the layouts of the attention
+//                    kernel.
+//   sm103_attention (MSA build, in sm103_kernels.cu): one launch per key chunk,
+//                    blockIdx.z picking heads 0-3 or 4-7 of an MSA row; the MSA
+//                    mask excludes keys per row through the pair-mask key bits;
+//                    each head's gated output u goes to global memory.
+//   sm103_msa_gemm<1>  the same GEMM for out = u W_o + b_o (f16 operands; all
+//                    256 output channels per CTA), the MSA mask (masked positions
+//                    are 0, or Ms with the residual) and the residual in the
+//                    epilogue.
 #include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -57,6 +60,19 @@ __device__ __forceinline__ void set_abort(volatile int* abort, uint32_t* status,
     atomicOr(status, code);
 }
 
+// (hi, lo) split of x in bf16: two 16-bit codes whose sum is x to ~2^-16
+__device__ __forceinline__ uint32_t split_bf16(float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+    return static_cast<uint32_t>(__bfloat16_as_ushort(h)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l)) << 16);
+}
+// the same in f16
+__device__ __forceinline__ uint32_t split_f16(float x) {
+    const __half h = __float2half_rn(x);
+    const __half l = __float2half_rn(x - __half2float(h));
+    return static_cast<uint32_t>(__half_as_ushort(h)) | (static_cast<uint32_t>(__half_as_ushort(l)) << 16);
+}
+
 // Block-uniform read of the device status word.
 __device__ __forceinline__ bool status_set(const uint32_t* status) {
     __shared__ int skip;
@@ -71,8 +87,8 @@ __device__ __forceinline__ bool status_set(const uint32_t* status) {
 struct MsaPrepArgs {
     const float *gm, *bm, *gz, *bz, *b_g, *b_o;
     const __nv_bfloat16 *w_q, *w_k, *w_v, *w_g, *w_b, *w_o;
-    __nv_bfloat16* wprep;   // [1024][256]: row n = (gamma_m . W)[:, n], K-major
-    float* cst;             // [512][4]: per column pair {colsum(n), colsum(n+1), off(n), off(n+1)}
+    __nv_bfloat16* wprep;   // [1024][256]: row n = (gamma_m . W)[:, n] (q columns x log2(e)/sqrt(d)), K-major
+    float* cst;             // [2][1024]: colsum of each column, then its offset
     float* wb;              // [128][8] gamma_z . W_b, then bcs[8] (column sums), bbw[8] (beta_z W_b)
     __half* wo_t;           // [256][256]: row n = W_o[:, n]
     float* bo;              // [256]
@@ -85,7 +101,8 @@ __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
     if (n < NPROJ) {
         const int grp = n / CH, col = n % CH;     // q | k | v | g
         const __nv_bfloat16* W = grp == 0 ? a.w_q : grp == 1 ? a.w_k : grp == 2 ? a.w_v : a.w_g;
-        const float wv = __bfloat162float(W[c * CH + col]);
+        const float sc = grp == 0 ? kLog2e * rsqrtf((float)HD) : 1.f;   // q carries log2(e) / sqrt(d)
+        const float wv = __bfloat162float(W[c * CH + col]) * sc;
         const __nv_bfloat16 r = __float2bfloat16_rn(a.gm[c] * wv);
         a.wprep[(size_t)n * CM + c] = r;
         float wr = __bfloat162float(r), bw = a.bm[c] * wv;
@@ -104,9 +121,8 @@ __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
                 cs += red[0][i];
                 b += red[1][i];
             }
-            const float sc = grp == 0 ? kLog2e * rsqrtf((float)HD) : 1.f;
-            a.cst[(n >> 1) * 4 + (n & 1)] = cs;
-            a.cst[(n >> 1) * 4 + 2 + (n & 1)] = b * sc + (grp == 3 ? a.b_g[col] : 0.f);
+            a.cst[n] = cs;
+            a.cst[NPROJ + n] = b + (grp == 3 ? a.b_g[col] : 0.f);
         }
     } else if (n < NPROJ + CM) {
         const int row = n - NPROJ;                // output channel of W_o
@@ -136,69 +152,171 @@ __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
 // =====================================================================================
 // Pair bias of the 8 heads: bias[h][i][j] = log2(e) * LN_z(Z[i, j]) . W_b[:, h]
 // =====================================================================================
-// One warp per pair (i, j) of the padded I_pad x I_pad grid.  Lane l holds channels
-// 4l .. 4l+3.  LN(z) . W_b = rstd * (z . (gamma W_b) - mu * colsum) + beta W_b.
+// One block per (row i, 64 keys j0 .. j0+63).  Z[i, j0 .. j0+63, :] is one contiguous
+// 16 KB run: it is staged in shared memory with coalesced 16-byte loads (rows padded
+// to 264 B, which keeps the per-pair 8-byte reads below at two wavefronts a warp).  Thread (pair p, head
+// pair hq) then forms the LayerNorm statistics of pair p (shifted by its first
+// channel) and two of the 8 dot products:
+//   LN(z) . W_b[:, h] = rstd * (z . (gamma W_b)[:, h] - mu * colsum_h) + (beta W_b)_h.
+// The 8 x 64 results are staged again and leave as one 128-byte run per head.
+namespace kb {
+constexpr int kPairs = 64;
+constexpr int kRowBytes = CZ * 2 + 8;        // 264
+}  // namespace kb
+
 __global__ void __launch_bounds__(256) sm103_msa_bias(const __nv_bfloat16* Z, int I, int I_pad, float eps,
                                                       const float* wb, __half* bias) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= I_pad * I_pad) return;
-    const int i = warp / I_pad, j = warp % I_pad;
-    float v = 0.f;
-    if (i < I && j < I) {
-        const uint2 raw = reinterpret_cast<const uint2*>(Z + ((size_t)i * I + j) * CZ)[lane];
-        float z[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
-        float s1 = z[0] + z[1] + z[2] + z[3];
-        for (int o = 16; o; o >>= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-        const float mu = s1 * (1.f / CZ);
-        float s2 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s2 = fmaf(z[e] - mu, z[e] - mu, s2);
-        for (int o = 16; o; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-        const float rstd = rsqrtf(s2 * (1.f / CZ) + eps);
-        const float* bcs = wb + CZ * HM;
-        const float* bbw = bcs + HM;
-        float part[HM];
-#pragma unroll
-        for (int h = 0; h < HM; ++h) {
-            float acc = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc = fmaf(z[e], wb[(4 * lane + e) * HM + h], acc);
-            part[h] = acc;
+    __shared__ __align__(16) uint8_t zt[kb::kPairs * kb::kRowBytes];
+    __shared__ __align__(16) float wq[4][CZ][2];           // (gamma_z W_b) by head pair
+    __shared__ __align__(16) __half ob[HM][kb::kPairs];
+    const int tid = threadIdx.x;
+    const int i = blockIdx.y, j0 = blockIdx.x * kb::kPairs;
+    if (i >= I) {                                          // padded query rows: 0
+        if (tid < HM * 8) {
+            const int h = tid >> 3, c = tid & 7;
+            reinterpret_cast<uint4*>(bias + ((size_t)h * I_pad + i) * I_pad + j0)[c] = make_uint4(0, 0, 0, 0);
         }
-#pragma unroll
-        for (int h = 0; h < HM; ++h)
-            for (int o = 16; o; o >>= 1) part[h] += __shfl_xor_sync(0xffffffffu, part[h], o);
-        if (lane < HM) {
-            float dot = part[0];
-#pragma unroll
-            for (int h = 1; h < HM; ++h)
-                if (lane == h) dot = part[h];
-            v = (rstd * (dot - mu * bcs[lane]) + bbw[lane]) * kLog2e;
-        }
-    } else if (i < I) {
-        v = kMaskedBias;                         // padded key
+        return;
     }
-    if (lane < HM) bias[((size_t)lane * I_pad + i) * I_pad + j] = __float2half_rn(v);
+    const int nj = I - j0 < kb::kPairs ? I - j0 : kb::kPairs;   // valid keys in this block (may be <= 0)
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(Z + ((size_t)i * I + j0) * CZ);
+        for (int q = tid; q < kb::kPairs * (CZ / 8); q += 256) {
+            const int pr = q >> 4, c = q & 15;                 // 16 x 16 B per pair
+            const uint4 v = pr < nj ? src[q] : make_uint4(0, 0, 0, 0);
+            uint2* dst = reinterpret_cast<uint2*>(zt + pr * kb::kRowBytes + c * 16);   // rows are 8-byte aligned
+            dst[0] = make_uint2(v.x, v.y);
+            dst[1] = make_uint2(v.z, v.w);
+        }
+        for (int q = tid; q < CZ * HM; q += 256) {
+            const int c = q / HM, h = q % HM;
+            wq[h >> 1][c][h & 1] = wb[q];
+        }
+    }
+    __syncthreads();
+    const int pr = tid & 63, hq = tid >> 6;
+    const uint8_t* row = zt + pr * kb::kRowBytes;
+    const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(row));
+    float sd = 0.f, sq = 0.f, d0 = 0.f, d1 = 0.f;
+#pragma unroll 8
+    for (int c4 = 0; c4 < CZ / 4; ++c4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row + c4 * 8);
+        const float z[4] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 wv = *reinterpret_cast<const float2*>(&wq[hq][c4 * 4 + e][0]);
+            const float dz = z[e] - shift;
+            sd += dz;
+            sq = fmaf(dz, dz, sq);
+            d0 = fmaf(z[e], wv.x, d0);
+            d1 = fmaf(z[e], wv.y, d1);
+        }
+    }
+    const float md = sd * (1.f / CZ);
+    const float mu = shift + md;
+    const float rstd = rsqrtf(fmaxf(sq * (1.f / CZ) - md * md, 0.f) + eps);
+    const float* bcs = wb + CZ * HM;
+    const float* bbw = bcs + HM;
+    const int h = 2 * hq;
+    const bool valid = pr < nj;
+    ob[h][pr] = __float2half_rn(valid ? (rstd * (d0 - mu * bcs[h]) + bbw[h]) * kLog2e : kMaskedBias);
+    ob[h + 1][pr] = __float2half_rn(valid ? (rstd * (d1 - mu * bcs[h + 1]) + bbw[h + 1]) * kLog2e : kMaskedBias);
+    __syncthreads();
+    if (tid < HM * 8) {
+        const int hh = tid >> 3, c = tid & 7;
+        reinterpret_cast<uint4*>(bias + ((size_t)hh * I_pad + i) * I_pad + j0)[c] =
+            reinterpret_cast<const uint4*>(&ob[hh][0])[c];
+    }
 }
 
 // =====================================================================================
-// Row GEMM: [128 rows x K = 256] x [256 x 128-column block], persistent per block
+// LayerNorm_m statistics of every (row, residue) slot: rowstat[s * I_pad + i] = (mu, rstd)
 // =====================================================================================
+// One warp per 4 consecutive slots (2 KB of Ms, its four 16-byte loads a lane issued
+// together); lane l holds channels 8l .. 8l+7 of each.  Sums are shifted by the
+// slot's first channel.  Padded residues (i >= I) get (0, 1), which makes their
+// projections the plain offsets (finite; they are never attended to).
+constexpr int kStatSlots = 4;
+
+__global__ void __launch_bounds__(256) sm103_msa_ln_stats(const __nv_bfloat16* M, int S, int I, int I_pad, float eps,
+                                                          float2* rowstat, uint4* axrow) {
+    const long long slot0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kStatSlots;
+    const int lane = threadIdx.x & 31;
+    const long long n_slots = (long long)S * I_pad;
+    uint4 v[kStatSlots];
+    bool live[kStatSlots];
+#pragma unroll
+    for (int k = 0; k < kStatSlots; ++k) {
+        const long long slot = slot0 + k;
+        const int s = (int)(slot / I_pad), i = (int)(slot % I_pad);
+        live[k] = slot < n_slots && i < I;
+        v[k] = live[k] ? reinterpret_cast<const uint4*>(M + ((size_t)s * I + i) * CM)[lane] : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kStatSlots; ++k) {
+        const float shift = __shfl_sync(0xffffffffu, bf16lo(v[k].x), 0);
+        const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        float sd = 0.f, sq = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float a = bf16lo(w4[q]) - shift, b = bf16hi(w4[q]) - shift;
+            sd += a + b;
+            sq = fmaf(a, a, fmaf(b, b, sq));
+        }
+        for (int o = 16; o; o >>= 1) {
+            sd += __shfl_xor_sync(0xffffffffu, sd, o);
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        }
+        if (lane == k && slot0 + k < n_slots) {
+            const float md = sd * (1.f / CM);
+            const float mu = live[k] ? shift + md : 0.f;
+            const float var = fmaxf(sq * (1.f / CM) - md * md, 0.f) + eps;
+            rowstat[slot0 + k] = make_float2(mu, live[k] ? rsqrtf(var) : 1.f);
+            // the slot's row of the projection's LayerNorm K-step: (-mu, -mu, sd, sd) as
+            // bf16 (hi, lo) pairs, sd = sqrt(var) = 1 / rstd
+            const uint32_t m2 = split_bf16(-mu), s2 = split_bf16(live[k] ? sqrtf(var) : 1.f);
+            axrow[slot0 + k] = make_uint4(m2, m2, s2, s2);
+        }
+    }
+}
+
+// =====================================================================================
+// Row GEMM: [128 slots x K = 256] x [256 x 256 columns], persistent per block
+// =====================================================================================
+// One block owns 256 output columns (its 128 KB of K-major weights resident in
+// shared memory) and walks 128-slot tiles.  N = 256 per MMA keeps the tensor
+// core's shared-memory operand reads at 12 KB per 128 x 256 x 16 step (an N = 128
+// step reads 8 KB for half the work, and with the TMA writes of A that saturates
+// shared-memory bandwidth).  A arrives in K-chunks of 64 (16 KB) through a ring of
+// 5 slots.  Per-column terms enter through one more K-step: a 16-wide A tile per
+// 128 slots (`ax`) against a 16-wide B tile per column (`bx`), bf16 / f16 values
+// split into a high and a low part so that the products are exact to ~2^-16:
+//   MODE 0  ax = (-mu, -mu, sd, sd) as (hi, lo, hi, lo, ...), bx = (cs, cs, off, off)
+//           so the accumulator holds m W' - mu cs + sd off and the epilogue
+//           multiplies by rstd = 1 / sd: LN(m) W = rstd (m W' - mu cs) + off.
+//   MODE 1  ax = (1, 1, 0, ...), bx = (b_o hi, b_o lo, 0, ...): the output bias.
+// The epilogue (8 warps: two per TMEM lane quadrant, 128 columns each) stores
+// straight from registers, so shared memory carries only operands.
 namespace kg {
-constexpr int kThreads = 256;                // warp 0 TMA producer, warp 1 MMA issuer, warps 4-7 epilogue
-constexpr int kB = 0;                        // B block: 4 K-chunks x [128 rows x 128 B] (SW128), 64 KB
-constexpr int kA = 65536;                    // A stages: 2 x 4 K-chunks x [128 rows x 128 B] (SW128)
-constexpr int kABytes = 65536;
-constexpr int kBar = kA + 2 * kABytes;
+constexpr int kThreads = 384;                // warp 0 producer, warp 1 MMA issuer, warps 4-11 epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kSlots = 5;                    // A ring: 5 x [128 rows x 64 K] (SW128)
+constexpr int kB = 0;                        // B: 4 K-chunks x [256 rows x 128 B] (SW128), 128 KB
+constexpr int kA = 131072;
+constexpr int kBX = kA + kSlots * 16384;     // bx: 256 rows x 16 B (no swizzle)
+constexpr int kAX = kBX + 4096;              // ax: 2 x [128 rows x 16 B]
+constexpr int kZero = kAX + 4096;            // 4 KB of zeros: K columns 8 .. 15 of ax and bx
+constexpr int kBar = kZero + 4096;
 constexpr int kSmem = kBar + 256 + 1024;
 static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
+static_assert(kA % 1024 == 0 && kBX % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 }  // namespace kg
 
 struct GemmParams {
-    int S, I, I_pad, n_tiles;                // tiles of 128 (row, residue) positions over S x I_pad
-    float eps;
-    const float* cst;                        // mode 0
+    int S, I, I_pad, n_tiles;                // tiles of 128 (row, residue) slots over S x I_pad
+    const float* cst;                        // mode 0: [2][1024] column sums, then offsets
+    const float2* rowstat;                   // mode 0: (mu, rstd) per slot
+    const uint4* axrow;                      // mode 0: the slot's row of the LayerNorm K-step
     __half *q, *k, *vt, *g;                  // mode 0 outputs
     const float* bo;                         // mode 1
     const uint8_t* mask;                     // mode 1: [S, I] or NULL
@@ -208,9 +326,10 @@ struct GemmParams {
 };
 
 // MODE 0: the MSA projection (A = Ms, bf16, through a 3-D map [S][I][256] whose
-// residue extent zero-fills the padded positions; epilogue: LayerNorm fold, q / k /
-// v^T / gate).  MODE 1: the output projection (A = u, f16, [S * I_pad][256];
-// epilogue: + b_o, MSA mask, residual, bf16 store).
+// residue extent zero-fills the padded slots; block x = 0 q, 1 k, 2 v, 3 gate;
+// epilogue: rstd x accumulator, sigmoid for the gate, q / k / gate as
+// [S][8][I_pad][32], v^T as [S][8][32][I_pad]).  MODE 1: the output projection
+// (A = u, f16, [S * I_pad][256]; epilogue: MSA mask, residual, bf16 out [S][I][256]).
 template <int MODE>
 __global__ void __launch_bounds__(kg::kThreads, 1)
 sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, GemmParams p) {
@@ -219,30 +338,55 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kg::kBar);
     uint64_t* b_full = bars + 0;
-    uint64_t* a_full = bars + 1;      // [2]
-    uint64_t* a_empty = bars + 3;     // [2]: the MMA's commit (+ the 4 epilogue warps in MODE 0)
-    uint64_t* acc_full = bars + 5;    // [2]
-    uint64_t* acc_empty = bars + 7;   // [2]: 4 epilogue warps
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
-    volatile int* abort = reinterpret_cast<volatile int*>(bars + 10);
-    uint64_t* mma_done = bars + 11;   // every MMA of this block retired (before the TMEM is freed)
+    uint64_t* a_full = bars + 1;      // [5]
+    uint64_t* a_empty = bars + 6;     // [5]: the MMA's commit
+    uint64_t* acc_full = bars + 11;   // [2]
+    uint64_t* acc_empty = bars + 13;  // [2]: the 8 epilogue warps
+    uint64_t* ax_empty = bars + 15;   // [2]: MODE 0, the MMA's commit after the tile
+    uint64_t* mma_done = bars + 17;   // every MMA of this block retired (before the TMEM is freed)
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
+    volatile int* abort = reinterpret_cast<volatile int*>(bars + 19);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cb = blockIdx.x;                // 128-column block of the output
+    const int grp = blockIdx.x;               // MODE 0: 0 q, 1 k, 2 v, 3 gate
     const int tpl = p.I_pad / 128;            // tiles per MSA row
     if (threadIdx.x == 0) {
         mbar_init(b_full, 1);
+        for (int q = 0; q < kg::kSlots; ++q) {
+            mbar_init(a_full + q, 1);
+            mbar_init(a_empty + q, 1);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(a_full + s, 1);
-            mbar_init(a_empty + s, MODE == 0 ? 5 : 1);
             mbar_init(acc_full + s, 1);
-            mbar_init(acc_empty + s, 4);
+            mbar_init(acc_empty + s, kg::kEpiWarps);
+            mbar_init(ax_empty + s, 1);
         }
         mbar_init(mma_done, 1);
         *abort = 0;
         fence_mbar_init();
     }
+    for (int i = threadIdx.x; i < 4096 / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(sm + kg::kZero)[i] = make_uint4(0, 0, 0, 0);
+    if (warp >= 4) {
+        const int c = threadIdx.x - 128;      // column 0 .. 255 of this block: its bx row
+        uint4 row;
+        if (MODE == 0) {
+            const int n = grp * 256 + c;
+            const uint32_t cs = split_bf16(p.cst[n]), of = split_bf16(p.cst[NPROJ + n]);
+            row = make_uint4((cs & 0xFFFFu) * 0x10001u, (cs >> 16) * 0x10001u, (of & 0xFFFFu) * 0x10001u,
+                             (of >> 16) * 0x10001u);                 // (cs_h, cs_h, cs_l, cs_l, of_h, of_h, of_l, of_l)
+        } else {
+            row = make_uint4(split_f16(p.bo[c]), 0u, 0u, 0u);        // (bo_h, bo_l, 0, ...)
+            if (c < 128) {                                           // ax of both buffers: (1, 1, 0, ...) in f16
+                const uint4 one = make_uint4(0x3C003C00u, 0u, 0u, 0u);
+                reinterpret_cast<uint4*>(sm + kg::kAX)[c] = one;
+                reinterpret_cast<uint4*>(sm + kg::kAX + 2048)[c] = one;
+            }
+        }
+        reinterpret_cast<uint4*>(sm + kg::kBX)[c] = row;
+    }
+    fence_proxy_async_smem();
     if (warp == 1) {
-        tmem_alloc(tmem_holder, 256);
+        tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -250,40 +394,56 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
+    // Register split: launched at 168 per thread; the control warpgroup (warps 0-3)
+    // drops to 80 and the two epilogue warpgroups grow to 208 (128 x 80 + 256 x 208
+    // = 63488 <= 384 x 168), room for a whole 128-column row of the accumulator.
+    if (warp < 4) setmaxnreg_dec<80>();
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        int issued = 0;
+        // ------------------------------------------------------------ producer: TMA of A and B, the ax tiles
+        int issued = 0;                       // A chunks issued (chunk c of the block goes to slot c % 5)
         bool ok = true;
         if (lane == 0) {
             prefetch_tmap(&mapA);
             prefetch_tmap(&mapB);
-            mbar_arrive_expect_tx(b_full, 65536);
-            for (int kc = 0; kc < 4; ++kc) tma_load_2d(sm + kg::kB + kc * 16384, &mapB, b_full, kc * 64, cb * 128);
-            int j = 0;
-            for (int t = blockIdx.y; t < p.n_tiles; t += gridDim.y, ++j) {
-                const int st = j & 1;
-                if (!mbar_wait(a_empty + st, ((j >> 1) & 1) ^ 1, abort)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* dst = sm + kg::kA + st * kg::kABytes;
-                mbar_arrive_expect_tx(a_full + st, kg::kABytes);
-                if (MODE == 0) {
-                    const int s = t / tpl, i0 = (t % tpl) * 128;
-                    for (int kc = 0; kc < 4; ++kc) tma_load_3d(dst + kc * 16384, &mapA, a_full + st, kc * 64, i0, s);
-                } else {
-                    for (int kc = 0; kc < 4; ++kc) tma_load_2d(dst + kc * 16384, &mapA, a_full + st, kc * 64, t * 128);
-                }
-                issued = j + 1;
+            mbar_arrive_expect_tx(b_full, 131072);
+            for (int kc = 0; kc < 4; ++kc) tma_load_2d(sm + kg::kB + kc * 32768, &mapB, b_full, kc * 64, grp * 256);
+        }
+        int j = 0;
+        for (int t = blockIdx.y; ok && t < p.n_tiles; t += gridDim.y, ++j) {
+            const int s = t / tpl, i0 = (t % tpl) * 128;
+            // ax of this tile (MODE 0: buffer j & 1, free once the MMAs of tile j - 2
+            // retired) rides on the barrier of the tile's first A chunk
+            if (MODE == 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(ax_empty + (j & 1), ((j >> 1) & 1) ^ 1, abort));
+                if (!ok) break;
             }
+            for (int kc = 0; kc < 4; ++kc) {
+                const int q = issued % kg::kSlots, n = issued / kg::kSlots;
+                ok = __all_sync(0xffffffffu, mbar_wait(a_empty + q, (n & 1) ^ 1, abort));
+                if (!ok) break;
+                if (lane == 0) {
+                    uint8_t* dst = sm + kg::kA + q * 16384;
+                    const bool with_ax = MODE == 0 && kc == 0;
+                    mbar_arrive_expect_tx(a_full + q, 16384 + (with_ax ? 2048 : 0));
+                    if (with_ax) bulk_load(sm + kg::kAX + (j & 1) * 2048, p.axrow + (size_t)t * 128, 2048, a_full + q);
+                    if (MODE == 0)
+                        tma_load_3d(dst, &mapA, a_full + q, kc * 64, i0, s);
+                    else
+                        tma_load_2d(dst, &mapA, a_full + q, kc * 64, t * 128);
+                }
+                __syncwarp();
+                ++issued;
+            }
+        }
+        if (lane == 0) {
             volatile int keep_waiting = 0;
             mbar_wait(b_full, 0, &keep_waiting);
             if (!ok) {
                 set_abort(abort, p.status, kStatusTimeoutProducer);
-                // the last copy into each A stage lands before the block ends
-                for (int st = 0; st < 2; ++st) {
-                    const int jl = issued - 1 - ((issued - 1 - st) % 2 + 2) % 2;
-                    if (jl >= 0) mbar_wait(a_full + st, (jl >> 1) & 1, &keep_waiting);
+                // the last copy into each A slot lands before the block ends
+                for (int q = 0; q < kg::kSlots; ++q) {
+                    const int cl = issued - 1 - ((issued - 1 - q) % kg::kSlots + kg::kSlots) % kg::kSlots;
+                    if (cl >= 0) mbar_wait(a_full + q, (cl / kg::kSlots) & 1, &keep_waiting);
                 }
             }
         }
@@ -291,25 +451,41 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = MODE == 0 ? idesc_bf16_f32(128, 128) : idesc_f16_f32(128, 128);
+            constexpr uint32_t idesc = MODE == 0 ? idesc_bf16_f32(128, 256) : idesc_f16_f32(128, 256);
             bool ok = mbar_wait(b_full, 0, abort);
-            int j = 0;
+            const uint32_t bbase = smem_u32(sm + kg::kB);
+            const uint32_t zero = smem_u32(sm + kg::kZero), bx = smem_u32(sm + kg::kBX);
+            const uint64_t bxd = sdesc_noswizzle(bx, zero - bx, 128);
+            int used = 0, j = 0;
             for (int t = blockIdx.y; ok && t < p.n_tiles; t += gridDim.y, ++j) {
-                const int st = j & 1, ab = j & 1;
-                if (!mbar_wait(a_full + st, (j >> 1) & 1, abort) || !mbar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, abort)) {
+                const int ab = j & 1;
+                if (!mbar_wait(acc_empty + ab, ((j >> 1) & 1) ^ 1, abort)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t abase = smem_u32(sm + kg::kA + st * kg::kABytes), bbase = smem_u32(sm + kg::kB);
+                for (int kc = 0; kc < 4; ++kc, ++used) {
+                    const int q = used % kg::kSlots, n = used / kg::kSlots;
+                    if (!mbar_wait(a_full + q, n & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (kc == 0) {                                  // the per-column terms
+                        const uint32_t ax = smem_u32(sm + kg::kAX + (MODE == 0 ? (j & 1) * 2048 : 0));
+                        mma_ss(tmem + ab * 256, sdesc_noswizzle(ax, zero - ax, 128), bxd, idesc, 0u);
+                    }
+                    const uint32_t abase = smem_u32(sm + kg::kA + q * 16384);
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t ad = sdesc(abase + (kk >> 2) * 16384 + (kk & 3) * 32, 1024, kSwizzle128);
-                    const uint64_t bd = sdesc(bbase + (kk >> 2) * 16384 + (kk & 3) * 32, 1024, kSwizzle128);
-                    mma_ss(tmem + ab * 128, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc(abase + kk * 32, 1024, kSwizzle128);
+                        const uint64_t bd = sdesc(bbase + kc * 32768 + kk * 32, 1024, kSwizzle128);
+                        mma_ss(tmem + ab * 256, ad, bd, idesc, 1u);
+                    }
+                    tc_commit(a_empty + q);
                 }
+                if (!ok) break;
+                if (MODE == 0) tc_commit(ax_empty + (j & 1));
                 tc_commit(acc_full + ab);
-                tc_commit(a_empty + st);
             }
             if (!ok) set_abort(abort, p.status, kStatusTimeoutMma);
             tc_commit(mma_done);
@@ -318,127 +494,100 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------------------------------ epilogue (one thread per row)
-        const int wq = warp - 4;
+        setmaxnreg_inc<208>();
+        // ------------------------------------------------------------ epilogue: thread = slot, 128 columns
+        // The 128 columns come out of TMEM in two x64 loads and one wait per tile
+        // (a TMEM load waits about as long as the tensor core keeps TMEM busy, so
+        // one wait per tile instead of one per 32 columns).
+        const int wq = warp & 3, half = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + half * 128;
+        float rstd = 1.f;
+        bool valid = false;
+        auto fetch = [&](int t) {             // this slot's operand of tile t
+            if (t >= p.n_tiles) return;
+            if (MODE == 0) {
+                rstd = p.rowstat[(size_t)t * 128 + r].y;
+            } else {
+                const int s = t / tpl, i = (t % tpl) * 128 + r;
+                valid = i < p.I && (p.mask == nullptr || p.mask[(size_t)s * p.I + i] != 0);
+            }
+        };
+        fetch(blockIdx.y);
         int j = 0;
         bool ok = true;
         for (int t = blockIdx.y; t < p.n_tiles; t += gridDim.y, ++j) {
-            const int st = j & 1, ab = j & 1;
+            const int ab = j & 1;
             const int s = t / tpl, i = (t % tpl) * 128 + r;
-            float mu = 0.f, rstd = 0.f;
-            if (MODE == 0) {
-                // LayerNorm statistics of this row from the staged tile (4 K-chunks of 128 B),
-                // shifted by its first channel
-                if (!mbar_wait(a_full + st, (j >> 1) & 1, abort)) { ok = false; break; }
-                const uint8_t* row = sm + kg::kA + st * kg::kABytes + r * 128;
-                const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(row + ((0 ^ (r & 7)) << 4)));
-                float sd = 0.f, sq = 0.f;
-#pragma unroll 4
-                for (int cc = 0; cc < 32; ++cc) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(row + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const float d0 = bf16lo(w4[q2]) - shift, d1 = bf16hi(w4[q2]) - shift;
-                        sd += d0 + d1;
-                        sq = fmaf(d0, d0, fmaf(d1, d1, sq));
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(a_empty + st);
-                const float md = sd * (1.f / CM);
-                mu = shift + md;
-                rstd = rsqrtf(fmaxf(sq * (1.f / CM) - md * md, 0.f) + p.eps);
-            }
+            const float cur_rstd = rstd;
+            const bool cur_valid = valid;
             if (!mbar_wait(acc_full + ab, (j >> 1) & 1, abort)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t tacc = tl + ab * 128;
-            if (MODE == 0) {
-                const int grp = cb >> 1;                 // 0 q, 1 k, 2 v, 3 gate
-                const float rr = grp == 0 ? rstd * (kLog2e * rsqrtf((float)HD)) : rstd;
-                const float nmu = -mu;
-#pragma unroll 1
-                for (int hh = 0; hh < 4; ++hh) {
-                    const int head = (cb & 1) * 4 + hh;
-                    uint32_t acc[32];
-                    tmem_ld32(tacc + hh * 32, acc);
-                    tmem_ld_wait();
-                    const float4* cst = reinterpret_cast<const float4*>(p.cst) + ((cb * 128 + hh * 32) >> 1);
+            uint32_t acc[2][64];
+            tmem_ld64(tl + ab * 256, acc[0]);
+            tmem_ld64(tl + ab * 256 + 64, acc[1]);
+            tmem_ld_wait();
+            tmem_regs_ready(acc[0]);
+            tmem_regs_ready(acc[1]);
+            tc_fence_before();                                   // the accumulator is in registers
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + ab);
+            fetch(t + gridDim.y);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                const uint32_t* a = &acc[hh >> 1][(hh & 1) * 32];
+                if (MODE == 0) {
                     uint32_t o[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const float4 c = cst[e >> 1];
-                        float t0, t1, v0, v1;
-                        fma2(t0, t1, nmu, nmu, c.x, c.y, __uint_as_float(acc[e]), __uint_as_float(acc[e + 1]));
-                        fma2(v0, v1, rr, rr, t0, t1, c.z, c.w);
-                        if (grp == 3) {                   // sigmoid(v) = 0.5 tanh(v / 2) + 0.5
-                            v0 = fmaf(0.5f, tanh_approx(0.5f * v0), 0.5f);
-                            v1 = fmaf(0.5f, tanh_approx(0.5f * v1), 0.5f);
-                        }
-                        o[e >> 1] = pack_f16(v0, v1);
+                        const float v0 = cur_rstd * __uint_as_float(a[e]), v1 = cur_rstd * __uint_as_float(a[e + 1]);
+                        o[e >> 1] = grp == 3 ? sigmoid_f16x2(v0, v1) : pack_f16(v0, v1);
                     }
-                    const size_t lh = (size_t)s * HM + head;
-                    if (grp == 2) {                       // v^T: [S][8][32][I_pad]
+                    const size_t lh = (size_t)s * HM + half * 4 + hh;
+                    if (grp == 2) {                              // v^T: [S][8][32][I_pad]
                         unsigned short* dst = reinterpret_cast<unsigned short*>(p.vt + lh * HD * p.I_pad + i);
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
                             dst[(size_t)e * p.I_pad] = static_cast<unsigned short>(o[e >> 1] & 0xFFFFu);
                             dst[(size_t)(e + 1) * p.I_pad] = static_cast<unsigned short>(o[e >> 1] >> 16);
                         }
-                    } else {                               // q, k, gate: [S][8][I_pad][32]
+                    } else {                                     // q, k, gate: [S][8][I_pad][32]
                         __half* base = grp == 0 ? p.q : grp == 1 ? p.k : p.g;
                         uint4* dst = reinterpret_cast<uint4*>(base + (lh * p.I_pad + i) * HD);
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4)
                             dst[c4] = make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
                     }
-                }
-            } else {
-                const bool row_ok = i < p.I;
-                const size_t pos = (size_t)s * p.I + i;
-                const bool valid = row_ok && (p.mask == nullptr || p.mask[pos] != 0);
-#pragma unroll 1
-                for (int cq = 0; cq < 4; ++cq) {
-                    uint32_t acc[32];
-                    tmem_ld32(tacc + cq * 32, acc);
-                    tmem_ld_wait();
-                    if (row_ok) {
-                        const int c0 = cb * 128 + cq * 32;
-                        uint32_t zr[16];
-                        if (p.resid) {
-                            const uint4* rp = reinterpret_cast<const uint4*>(p.resid + pos * CM + c0);
+                } else if (i < p.I) {
+                    const size_t pos = (size_t)s * p.I + i;
+                    const int c0 = half * 128 + hh * 32;
+                    uint32_t zr[16];
 #pragma unroll
-                            for (int c4 = 0; c4 < 4; ++c4) {
-                                const uint4 v = rp[c4];
-                                zr[4 * c4] = v.x;
-                                zr[4 * c4 + 1] = v.y;
-                                zr[4 * c4 + 2] = v.z;
-                                zr[4 * c4 + 3] = v.w;
-                            }
+                    for (int c = 0; c < 16; ++c) zr[c] = 0u;
+                    if (p.resid != nullptr) {
+                        const uint4* rp = reinterpret_cast<const uint4*>(p.resid + pos * CM + c0);
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const uint4 v = rp[c4];
+                            zr[4 * c4] = v.x;
+                            zr[4 * c4 + 1] = v.y;
+                            zr[4 * c4 + 2] = v.z;
+                            zr[4 * c4 + 3] = v.w;
                         }
-                        uint32_t o[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float a0 = valid ? __uint_as_float(acc[e]) + p.bo[c0 + e] : 0.f;
-                            float a1 = valid ? __uint_as_float(acc[e + 1]) + p.bo[c0 + e + 1] : 0.f;
-                            if (p.resid) {
-                                a0 += bf16lo(zr[e >> 1]);
-                                a1 += bf16hi(zr[e >> 1]);
-                            }
-                            o[e >> 1] = pack_bf16(a0, a1);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(p.out + pos * CM + c0);
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4)
-                            dst[c4] = make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
                     }
+                    uint32_t o[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float a0 = (cur_valid ? __uint_as_float(a[e]) : 0.f) + bf16lo(zr[e >> 1]);
+                        const float a1 = (cur_valid ? __uint_as_float(a[e + 1]) : 0.f) + bf16hi(zr[e >> 1]);
+                        o[e >> 1] = pack_bf16(a0, a1);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + pos * CM + c0);
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        dst[c4] = make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + ab);
         }
         if (!ok) set_abort(abort, p.status, kStatusTimeoutEpilogue);
     }
@@ -446,7 +595,7 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -503,43 +652,55 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
 
     // ---- pair bias of the 8 heads
     {
-        const long long warps = (long long)Ip * Ip;
         if (tm) tm->begin("sm103_msa_bias", s);
-        sm103_msa_bias<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.Z), I, Ip, a.eps,
-                                                                   f32(W.wb32), hf(W.bias));
+        sm103_msa_bias<<<dim3(Ip / kb::kPairs, Ip), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.Z), I, Ip, a.eps,
+                                                                f32(W.wb32), hf(W.bias));
+        if (tm) tm->end(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+
+    // ---- LayerNorm_m statistics of every slot
+    {
+        const long long warps = ((long long)S * Ip + kStatSlots - 1) / kStatSlots;
+        if (tm) tm->begin("sm103_msa_ln_stats", s);
+        sm103_msa_ln_stats<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.M), S, I, Ip,
+                                                                       a.eps, reinterpret_cast<float2*>(ws + W.rowstat),
+                                                                       reinterpret_cast<uint4*>(ws + W.axrow));
         if (tm) tm->end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
 
     const int n_tiles = S * (Ip / 128);
-    const int rows_per_block = num_sms_of_device() / 8 > 0 ? num_sms_of_device() / 8 : 1;
+    const int nsm = num_sms_of_device();
 
     // ---- projection GEMM: q | k | v^T | gate
     {
         CUtensorMap mA, mB;
-        if (!sm103_map3d_bf16(&mA, a.M, CM, I, S, (uint64_t)CM * 2, (uint64_t)I * CM * 2, 64, 128, 1) ||
-            !sm103_map2d(&mB, ws + W.wprep, CM, NPROJ, CM * 2, 64, 128, 128, true))
+        if (!sm103_map3d_bf16(&mA, a.M, CM, I, S, (uint64_t)CM * 2, (uint64_t)I * CM * 2, 64, 128, 1, 128) ||
+            !sm103_map2d(&mB, ws + W.wprep, CM, NPROJ, CM * 2, 64, 256, 128, true))
             return cudaErrorInvalidValue;
         GemmParams gp{};
         gp.S = S;
         gp.I = I;
         gp.I_pad = Ip;
         gp.n_tiles = n_tiles;
-        gp.eps = a.eps;
         gp.cst = f32(W.cst);
+        gp.rowstat = reinterpret_cast<const float2*>(ws + W.rowstat);
+        gp.axrow = reinterpret_cast<const uint4*>(ws + W.axrow);
         gp.q = hf(W.q);
         gp.k = hf(W.k);
         gp.vt = hf(W.v);
         gp.g = hf(W.g);
         gp.status = a.status;
-        dim3 grid(NPROJ / 128, rows_per_block < n_tiles ? rows_per_block : n_tiles);
+        const int rows = nsm / (NPROJ / 256) > 0 ? nsm / (NPROJ / 256) : 1;
+        dim3 grid(NPROJ / 256, rows < n_tiles ? rows : n_tiles);
         if (tm) tm->begin("sm103_msa_proj", s);
         sm103_msa_gemm<0><<<grid, kg::kThreads, kg::kSmem, s>>>(mA, mB, gp);
         if (tm) tm->end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
 
-    // ---- attention (two launches of four heads per key chunk), gated u to global memory
+    // ---- attention (one launch per key chunk), gated u to global memory
     {
         MsaAttnArgs m{S, I, Ip, a.key_chunks, hf(W.q), hf(W.k), hf(W.v), hf(W.g), hf(W.bias), hf(W.u),
                       W.o_run ? f32(W.o_run) : nullptr, W.lse_run ? f32(W.lse_run) : nullptr, a.msa_mask,
@@ -551,7 +712,7 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
     {
         CUtensorMap mA, mB;
         if (!sm103_map2d(&mA, ws + W.u, CH, (uint64_t)S * Ip, CH * 2, 64, 128, 128, false) ||
-            !sm103_map2d(&mB, ws + W.wo_t, CH, CM, CH * 2, 64, 128, 128, false))
+            !sm103_map2d(&mB, ws + W.wo_t, CH, CM, CH * 2, 64, 256, 128, false))
             return cudaErrorInvalidValue;
         GemmParams gp{};
         gp.S = S;
@@ -563,8 +724,7 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
         gp.resid = a.residual ? static_cast<const __nv_bfloat16*>(a.M) : nullptr;
         gp.out = static_cast<__nv_bfloat16*>(a.out);
         gp.status = a.status;
-        const int rpb = num_sms_of_device() / 2;
-        dim3 grid(CM / 128, rpb < n_tiles ? rpb : n_tiles);
+        dim3 grid(1, nsm < n_tiles ? nsm : n_tiles);
         if (tm) tm->begin("sm103_msa_out", s);
         sm103_msa_gemm<1><<<grid, kg::kThreads, kg::kSmem, s>>>(mA, mB, gp);
         if (tm) tm->end(s);

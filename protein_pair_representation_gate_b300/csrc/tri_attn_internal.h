@@ -45,6 +45,8 @@ struct Workspace {
     size_t wprep = 0, colsum = 0, betaw = 0, wb32 = 0, wo_t = 0, bo = 0;  // prepared weights (sm103)
     size_t cst = 0;                                          // per column pair {colsum x2, offset x2} (sm103)
     size_t kbits = 0;                                        // [I][I_pad / 64 + 1] key-valid bits per line (sm103)
+    size_t rowstat = 0;                                      // (mu, rstd) per MSA slot (sm103 MSA path)
+    size_t axrow = 0;                                        // 16 B per MSA slot: its LayerNorm K-step row
     size_t total = 0;
 };
 
@@ -142,11 +144,13 @@ constexpr Workspace sm103_msa_layout(int S, int I, int key_chunks) {
     size_t off = 0;
     auto take = [&off](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
     w.wprep = take((size_t)1024 * 256 * 2);           // (gamma_m . W)^T for q | k | v | g, bf16
-    w.cst = take((size_t)512 * 4 * 4);                // per column pair {colsum x2, offset x2}
+    w.cst = take((size_t)2 * 1024 * 4);               // column sums, then offsets, of the 1024 columns
     w.wb32 = take((size_t)128 * 8 * 4 + 2 * 8 * 4);   // gamma_z . W_b, its column sums, beta_z W_b
     w.wo_t = take((size_t)256 * 256 * 2);             // W_o^T, f16
     w.bo = take(256 * 4);
     w.kbits = take((size_t)S * (w.I_pad / 64 + 1) * 8);
+    w.rowstat = take(P * 8);
+    w.axrow = take(P * 16);
     w.q = take(P * 256 * 2);
     w.k = take(P * 256 * 2);
     w.v = take(P * 256 * 2);
@@ -175,7 +179,7 @@ cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTime
 bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
                  uint32_t box_rows, int swizzle_bytes, bool bf16);
 bool sm103_map3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
+                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes);
 
 // Chunk bounds shared by both paths: size = round_up(ceil(I / n), 8).
 inline int chunk_size(int I, int n) {
