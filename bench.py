@@ -293,16 +293,22 @@ def secondary_runs(pkg, dev, peak):
     from synth.device import inputs_to_device
     from synth.rng import uniform01
 
-    cases = [("masked_768", ("start", "end"), 1, None, 5),
-             ("single_chain_2752", ("start",), 1, None, 3),
-             ("single_chain_2752", ("start",), 8, None, 3),
-             ("complex_2048", ("start", "end"), 1, 0.8, 3)]
+    from dataclasses import replace
+    from synth.workloads import WORKLOADS
+    # (workload, nodes, key chunks, pair-mask density, iterations, dtype: None = the workload's, "tf32")
+    cases = [("masked_768", ("start", "end"), 1, None, 5, None),
+             ("single_chain_2752", ("start",), 1, None, 3, None),
+             ("single_chain_2752", ("start",), 8, None, 3, None),
+             ("complex_2048", ("start", "end"), 1, 0.8, 3, None),
+             ("complex_2048", ("start", "end"), 1, None, 3, "tf32")]
     res = []
-    for name, nodes, chunks, density, iters in cases:
-        inp = make_inputs(name)
-        wl = inp.workload
+    for name, nodes, chunks, density, iters, dtype in cases:
+        wl = WORKLOADS[name]
+        if dtype == "tf32":
+            wl = replace(wl, dtype="f32")             # fp32 storage of the same seeded values
+        inp = make_inputs(wl)
         t = inputs_to_device(inp, dev)
-        op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=chunks)
+        op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, dtype or wl.dtype, key_chunks=chunks)
         pm = None
         if density is not None:
             u = uniform01(wl.seed, 13, 0, wl.I * wl.I).reshape(wl.I, wl.I)
@@ -334,7 +340,7 @@ def secondary_runs(pkg, dev, peak):
         ms_fwd = e0.elapsed_time(e1) / (iters * len(nodes))
         tf = wl.attention_flops() / (ms_fwd * 1e-3) / 1e12
         att = sum(kms.get("sm103_attention", [0.0])) / (iters * len(nodes))
-        res.append({"workload": name, "I": wl.I, "nodes": list(nodes), "key_chunks": chunks,
+        res.append({"workload": name, "I": wl.I, "dtype": dtype or wl.dtype, "nodes": list(nodes), "key_chunks": chunks,
                     "pair_mask_density": density, "token_pads": wl.n_pad, "ms_per_forward": ms_fwd,
                     "tflops": tf, "frac_of_peak": tf / peak,
                     "attention_ms_per_forward": att,

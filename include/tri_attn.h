@@ -39,8 +39,8 @@
  *     library never frees them and keeps no pointer after a call returns.
  *   - Weights are stored [in, out] row-major (x W); head h owns channels
  *     h*d .. h*d+d-1 of q, k, v, g and of the rows of W_o.
- *   - "dtype" tensors are float32 when config.dtype == TRI_ATTN_F32 and bf16
- *     (raw 16-bit patterns) when config.dtype == TRI_ATTN_BF16.
+ *   - "dtype" tensors are float32 when config.dtype is TRI_ATTN_F32 or
+ *     TRI_ATTN_TF32 and bf16 (raw 16-bit patterns) when it is TRI_ATTN_BF16.
  *   - Calls validate their arguments on the host first; a validation error
  *     is returned synchronously and nothing is launched.
  *   - tri_attn_forward is asynchronous on the given stream (a cudaStream_t
@@ -71,12 +71,21 @@ typedef enum {
 } tri_attn_status;
 
 typedef enum { TRI_ATTN_STARTING = 0, TRI_ATTN_ENDING = 1 } tri_attn_node;
-typedef enum { TRI_ATTN_F32 = 0, TRI_ATTN_BF16 = 1 } tri_attn_dtype;
+/* Storage type of Z, the projection weights and out, and the arithmetic it selects:
+ *   F32   fp32 storage and fp32 arithmetic (CUDA-core kernels; the 1e-4 bound)
+ *   BF16  bf16 storage; tensor cores with f16/bf16 operands, fp32 accumulation
+ *   TF32  fp32 storage; tensor cores reading the LayerNorm/projection operands as
+ *         tf32 (10-bit significand), f16 attention operands, fp32 accumulation and
+ *         fp32 output: the ExtraMSA-style mode (OpenFold-TRT summary, Methodology:
+ *         TF32 for ExtraMSA).  Shapes the TF32 kernels do not cover run the fp32
+ *         CUDA-core kernels, which are at least as accurate. */
+typedef enum { TRI_ATTN_F32 = 0, TRI_ATTN_BF16 = 1, TRI_ATTN_TF32 = 2 } tri_attn_dtype;
 
 /* Kernel path a context runs (tri_attn_path). */
 typedef enum {
     TRI_ATTN_PATH_SIMT = 0,     /* fp32 CUDA-core kernels: any supported shape, f32 or bf16 storage */
-    TRI_ATTN_PATH_SM103 = 1     /* tcgen05/TMEM/TMA kernels: bf16, c_z = 128, H = 4, d = 32           */
+    TRI_ATTN_PATH_SM103 = 1,    /* tcgen05/TMEM/TMA kernels: bf16, c_z = 128, H = 4, d = 32           */
+    TRI_ATTN_PATH_SM103_TF32 = 2 /* the same with dtype TF32: fp32 storage, c_z = 128, H = 4, d = 32  */
 } tri_attn_path_kind;
 
 typedef struct {

@@ -6,7 +6,7 @@ include/tri_attn.h); this package is its Python binding.  torch provides
 device memory and streams only.
 """
 from ._binding import (
-    BF16, ENDING, F32, PATH_SIMT, PATH_SM103, STARTING, EXPORTS,
+    BF16, ENDING, F32, PATH_SIMT, PATH_SM103, PATH_SM103_TF32, STARTING, TF32, EXPORTS,
     TriAttn, TriAttnConfig, TriAttnError, load_library, status_string,
 )
 
@@ -17,7 +17,8 @@ class TriangleAttention:
     """A context plus a cached workspace: out = op(node, Z, mask, weights).
 
     Z, weights and mask are torch CUDA tensors laid out as tri_attn.h states
-    (bf16 storage as torch.bfloat16 or raw int16 bits).  Returns `out`.
+    (bf16 storage as torch.bfloat16 or raw int16 bits; fp32 storage for the
+    "f32" and "tf32" dtypes).  Returns `out`.
     """
 
     def __init__(self, c_z: int, heads: int, head_dim: int, I_max: int, dtype: str = "bf16",
@@ -91,4 +92,5 @@ class MSARowAttention:
 
 
 __all__ = ["TriangleAttention", "MSARowAttention", "MSA_WEIGHT_NAMES", "TriAttn", "TriAttnConfig", "TriAttnError", "load_library", "status_string",
-           "STARTING", "ENDING", "F32", "BF16", "PATH_SIMT", "PATH_SM103", "EXPORTS", "WEIGHT_NAMES"]
+           "STARTING", "ENDING", "F32", "BF16", "TF32", "PATH_SIMT", "PATH_SM103", "PATH_SM103_TF32", "EXPORTS",
+           "WEIGHT_NAMES"]

@@ -15,8 +15,9 @@ LIB_PATH = os.path.join(PKG, "libtriattn.so")
 
 OK, EINVAL, EUNSUPPORTED, ENOMEM, ECUDA, ETIMEOUT, ERANGE = range(7)
 STARTING, ENDING = 0, 1
-F32, BF16 = 0, 1
-PATH_SIMT, PATH_SM103 = 0, 1
+F32, BF16, TF32 = 0, 1, 2
+DTYPES = {"f32": F32, "bf16": BF16, "tf32": TF32}
+PATH_SIMT, PATH_SM103, PATH_SM103_TF32 = 0, 1, 2
 NODES = {"start": STARTING, "end": ENDING, STARTING: STARTING, ENDING: ENDING}
 
 EXPORTS = ("tri_attn_create", "tri_attn_destroy", "tri_attn_path", "tri_attn_workspace_bytes",
@@ -133,13 +134,13 @@ class TriAttnConfig:
     heads: int
     head_dim: int
     I_max: int
-    dtype: str = "bf16"          # "f32" or "bf16"
+    dtype: str = "bf16"          # "f32", "bf16" or "tf32" (fp32 storage, TF32 tensor-core arithmetic)
     ln_eps: float = 1e-5
     key_chunks: int = 1
     force_simt: bool = False
 
     def to_c(self) -> Config:
-        return Config(self.c_z, self.heads, self.head_dim, self.I_max, BF16 if self.dtype == "bf16" else F32,
+        return Config(self.c_z, self.heads, self.head_dim, self.I_max, DTYPES[self.dtype],
                       self.ln_eps, self.key_chunks, int(self.force_simt))
 
 

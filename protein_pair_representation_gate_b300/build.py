@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libtriattn.so")
-SOURCES = ["tri_attn_api.cu", "simt_kernels.cu", "sm103_kernels.cu", "sm103_msa.cu", "tri_attn_static.cu"]
+SOURCES = ["tri_attn_api.cu", "simt_kernels.cu", "sm103_kernels.cu", "sm103_msa.cu", "sm103_tf32.cu", "tri_attn_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

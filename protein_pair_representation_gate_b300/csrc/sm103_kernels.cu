@@ -426,8 +426,8 @@ struct AttnParams {
     const __half* g;
     const float* bo;
     float *o_run, *lse_run;
-    const __nv_bfloat16* Z;    // residual source (NULL: write the update only); may equal out
-    __nv_bfloat16* out;
+    const void* Z;             // residual source (NULL: write the update only); may equal out
+    void* out;                 // bf16, or fp32 in the kF32 build
     uint32_t* status;
 };
 
@@ -498,7 +498,8 @@ static_assert(kBias % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 10
 // heads per line), the MSA mask arrives as the pair mask's key bits, and each
 // head's gated output goes to global memory for the separate output projection
 // (no W_o, no epilogue here).
-template <bool kEx, bool kMsa>
+// kF32: Z (residual) and out are fp32 (the TF32 forward); otherwise bf16.
+template <bool kEx, bool kMsa, bool kF32 = false>
 __global__ void __launch_bounds__(k2::kThreads, 1)
 sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapVt, const __grid_constant__ CUtensorMap mapB,
@@ -517,14 +518,15 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     if (p.mask != nullptr && p.mask[L] == 0) {
         // the whole line is padding: its update is zero (with a residual: out = Z)
         if (p.last && (!kEx || p.Z != p.out)) {
-            const size_t sL = p.node == TRI_ATTN_STARTING ? (size_t)p.I * CZ : CZ;
-            const size_t sX = p.node == TRI_ATTN_STARTING ? CZ : (size_t)p.I * CZ;
-            for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
-                const int x = xq0 + i / 16;
+            constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
+            const size_t sL = p.node == TRI_ATTN_STARTING ? (size_t)p.I : 1;
+            const size_t sX = p.node == TRI_ATTN_STARTING ? 1 : (size_t)p.I;
+            for (int i = threadIdx.x; i < 256 * kRow; i += blockDim.x) {
+                const int x = xq0 + i / kRow;
                 if (x < p.I) {
-                    const size_t at = L * sL + x * sX;
-                    reinterpret_cast<uint4*>(p.out + at)[i % 16] =
-                        (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z + at)[i % 16] : make_uint4(0, 0, 0, 0);
+                    const size_t at = (L * sL + x * sX) * kRow + i % kRow;
+                    reinterpret_cast<uint4*>(p.out)[at] =
+                        (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z)[at] : make_uint4(0, 0, 0, 0);
                 }
             }
         }
@@ -1078,40 +1080,58 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const size_t pair = p.node == TRI_ATTN_STARTING ? (size_t)L * p.I + x : (size_t)x * p.I + L;
                 const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0) &&
                                    (!kEx || p.pmask == nullptr || p.pmask[pair] != 0);
-                uint4* dst = reinterpret_cast<uint4*>(p.out + pair * CZ);
-                const uint4* zres = (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z + pair * CZ) : nullptr;
+                constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
+                uint4* dst = reinterpret_cast<uint4*>(p.out) + pair * kRow;
+                const uint4* zres = (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z) + pair * kRow : nullptr;
                 const uint32_t tOut = tl + k2::colS(g, 0);
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t v[32];
                     tmem_ld32(tOut + cb * 32, v);
                     tmem_ld_wait();
-                    uint32_t zw[16];                     // residual (this thread's own pair: read before write)
-                    if constexpr (kEx) {
+                    tmem_regs_ready(v);
+                    if constexpr (kF32) {
+                        // fp32 out (and residual): 32 channels = 8 16-byte words
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint4 zv = (zres && x < p.I) ? zres[cb * 4 + i] : make_uint4(0, 0, 0, 0);
-                            zw[4 * i] = zv.x;
-                            zw[4 * i + 1] = zv.y;
-                            zw[4 * i + 2] = zv.z;
-                            zw[4 * i + 3] = zv.w;
+                        for (int i = 0; i < 8; ++i) {
+                            float4 zv = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (kEx && zres && x < p.I) zv = *reinterpret_cast<const float4*>(zres + cb * 8 + i);
+                            const int e = 4 * i;
+                            const float4 r4 = make_float4(
+                                (valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f) + zv.x,
+                                (valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f) + zv.y,
+                                (valid ? __uint_as_float(v[e + 2]) + p.bo[cb * 32 + e + 2] : 0.f) + zv.z,
+                                (valid ? __uint_as_float(v[e + 3]) + p.bo[cb * 32 + e + 3] : 0.f) + zv.w);
+                            if (x < p.I) *reinterpret_cast<float4*>(dst + cb * 8 + i) = r4;
                         }
-                    }
-                    uint32_t o[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float a0 = valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f;
-                        float a1 = valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f;
+                    } else {
+                        uint32_t zw[16];                     // residual (this thread's own pair: read before write)
                         if constexpr (kEx) {
-                            a0 += bf16lo(zw[e >> 1]);
-                            a1 += bf16hi(zw[e >> 1]);
-                        }
-                        o[e >> 1] = pack_bf16(a0, a1);
-                    }
-                    if (x < p.I) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                            for (int i = 0; i < 4; ++i) {
+                                const uint4 zv = (zres && x < p.I) ? zres[cb * 4 + i] : make_uint4(0, 0, 0, 0);
+                                zw[4 * i] = zv.x;
+                                zw[4 * i + 1] = zv.y;
+                                zw[4 * i + 2] = zv.z;
+                                zw[4 * i + 3] = zv.w;
+                            }
+                        }
+                        uint32_t o[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float a0 = valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f;
+                            float a1 = valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f;
+                            if constexpr (kEx) {
+                                a0 += bf16lo(zw[e >> 1]);
+                                a1 += bf16hi(zw[e >> 1]);
+                            }
+                            o[e >> 1] = pack_bf16(a0, a1);
+                        }
+                        if (x < p.I) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                        }
                     }
                 }
             } else {
@@ -1210,15 +1230,6 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     if (!(attr_set.load(std::memory_order_acquire) & dev_bit)) {
         cudaError_t e = cudaFuncSetAttribute(sm103_ln_proj, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::kSmem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sm103_attention<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 k2::Lay<false>::kSmem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sm103_attention<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 k2::Lay<true>::kSmem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(sm103_attention<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 k2::Lay<true>::kSmem);
-        if (e != cudaSuccess) return e;
         attr_set.fetch_or(dev_bit, std::memory_order_release);
     }
 
@@ -1274,29 +1285,75 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     }
 
     // ---- attention (+ gate, output projection), once per key chunk
+    TriAttnLaunch l;
+    l.node = a.node;
+    l.I = I;
+    l.I_pad = Ip;
+    l.key_chunks = a.key_chunks;
+    l.inject = a.inject;
+    l.f32 = false;
+    l.mask = a.mask;
+    l.pair_mask = a.pair_mask;
+    l.Z_resid = a.residual ? a.Z : nullptr;
+    l.out = a.out;
+    l.q = hf(W.q);
+    l.k = hf(W.k);
+    l.vt = hf(W.v);
+    l.g = hf(W.g);
+    l.bias = hf(W.bias);
+    l.wo_t = hf(W.wo_t);
+    l.bo = f32(W.bo);
+    l.o_run = W.o_run ? f32(W.o_run) : nullptr;
+    l.lse_run = W.lse_run ? f32(W.lse_run) : nullptr;
+    l.kbits = reinterpret_cast<uint64_t*>(a.ws + W.kbits);
+    l.status = a.status;
+    return sm103_triangle_attention(l, s, tm);
+}
+
+cudaError_t sm103_triangle_attention(const TriAttnLaunch& l, cudaStream_t s, LaunchTimer* tm) {
+    const int I = l.I, Ip = l.I_pad;
+    static std::atomic<uint64_t> attr_set{0};
+    const int dev = current_device();
+    const uint64_t dev_bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (!(attr_set.load(std::memory_order_acquire) & dev_bit)) {
+        cudaError_t e = cudaFuncSetAttribute(sm103_attention<false, false, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, k2::Lay<false>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sm103_attention<true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     k2::Lay<true>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sm103_attention<false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     k2::Lay<false>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sm103_attention<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     k2::Lay<true>::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(dev_bit, std::memory_order_release);
+    }
     CUtensorMap mQ, mK, mV, mB, mWo;
     const uint64_t rows_qk = (uint64_t)I * NH * Ip;
-    if (!map2d(&mQ, hf(W.q), HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !map2d(&mK, hf(W.k), HD, rows_qk, HD * 2, HD, k2::kKT, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !map2d(&mV, hf(W.v), Ip, (uint64_t)I * NH * HD, (uint64_t)Ip * 2, 64, HD, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !map2d(&mB, hf(W.bias), Ip, (uint64_t)NH * Ip, (uint64_t)Ip * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !map2d(&mWo, hf(W.wo_t), CH, CZ, CH * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!map2d(&mQ, l.q, HD, rows_qk, HD * 2, HD, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mK, l.k, HD, rows_qk, HD * 2, HD, k2::kKT, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !map2d(&mV, l.vt, Ip, (uint64_t)I * NH * HD, (uint64_t)Ip * 2, 64, HD, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&mB, l.bias, Ip, (uint64_t)NH * Ip, (uint64_t)Ip * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&mWo, l.wo_t, CH, CZ, CH * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    cudaError_t e;
     uint64_t* kbits = nullptr;
-    if (a.pair_mask != nullptr) {
-        kbits = reinterpret_cast<uint64_t*>(a.ws + W.kbits);
+    if (l.pair_mask != nullptr) {
+        kbits = l.kbits;
         const int words = Ip / 64 + 1;
         if (tm) tm->begin("sm103_pair_keybits", s);
-        sm103_pair_keybits<<<(I * words + 127) / 128, 128, 0, s>>>(a.pair_mask, a.node, I, I, words, kbits);
+        sm103_pair_keybits<<<(I * words + 127) / 128, 128, 0, s>>>(l.pair_mask, l.node, I, I, words, kbits);
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const int cs = chunk_size(I, a.key_chunks);
+    const int cs = chunk_size(I, l.key_chunks);
     for (int k0 = 0; k0 < I; k0 += cs) {
         const int k1e = k0 + cs < I ? k0 + cs : I;
         AttnParams ap;
-        ap.node = a.node;
+        ap.node = l.node;
         ap.I = I;
         ap.I_pad = Ip;
         ap.k_begin = k0;
@@ -1304,24 +1361,32 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
         ap.nk = (k1e - k0 + k2::kKT - 1) / k2::kKT;
         ap.first = k0 == 0;
         ap.last = k1e == I;
-        ap.mask = a.mask;
-        ap.pmask = a.pair_mask;
+        ap.mask = l.mask;
+        ap.pmask = l.pair_mask;
         ap.kbits = kbits;
-        ap.Z = a.residual ? static_cast<const __nv_bfloat16*>(a.Z) : nullptr;
-        ap.g = hf(W.g);
-        ap.bo = f32(W.bo);
-        ap.o_run = W.o_run ? f32(W.o_run) : nullptr;
-        ap.lse_run = W.lse_run ? f32(W.lse_run) : nullptr;
-        ap.out = static_cast<__nv_bfloat16*>(a.out);
-        ap.status = a.status;
-        ap.inject = k0 == 0 ? a.inject : 0;
+        ap.Z = l.Z_resid;
+        ap.g = l.g;
+        ap.bo = l.bo;
+        ap.o_run = l.o_run;
+        ap.lse_run = l.lse_run;
+        ap.out = l.out;
+        ap.status = l.status;
+        ap.inject = k0 == 0 ? l.inject : 0;
         ap.u = nullptr;
         dim3 grid(Ip / 256, I);
+        const bool ex = ap.kbits != nullptr || ap.Z != nullptr;
         if (tm) tm->begin("sm103_attention", s);
-        if (ap.kbits != nullptr || ap.Z != nullptr)
-            sm103_attention<true, false><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
-        else
-            sm103_attention<false, false><<<grid, k2::kThreads, k2::Lay<false>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+        if (l.f32) {
+            if (ex)
+                sm103_attention<true, false, true><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+            else
+                sm103_attention<false, false, true><<<grid, k2::kThreads, k2::Lay<false>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+        } else {
+            if (ex)
+                sm103_attention<true, false><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+            else
+                sm103_attention<false, false><<<grid, k2::kThreads, k2::Lay<false>::kSmem, s>>>(mQ, mK, mV, mB, mWo, ap);
+        }
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1336,6 +1401,23 @@ bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                                                         : CU_TENSOR_MAP_SWIZZLE_NONE;
     return map2d(m, base, cols, rows, row_bytes, box_cols, box_rows, sw,
                  bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+bool sm103_map_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                   const uint32_t* box, int swizzle_bytes) {
+    auto fn = encode_fn();
+    if (!fn || rank < 1 || rank > 3) return false;
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        if (i > 0) st[i - 1] = strides[i - 1];
+    }
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(base), d, st, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool sm103_map3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,

@@ -162,6 +162,13 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (32-bit operands, K = 8 per instruction)
+__device__ __forceinline__ void mma_ss_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
 // Copy a 128-row x 32-byte operand tile (described like an MMA operand) from shared
 // memory to TMEM: row i -> lane i, its 32 bytes -> 8 consecutive columns.  Ordered
 // with this thread's later tcgen05.mma instructions.
@@ -189,6 +196,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // Same with f16 A and B.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4)                              // D format: f32 (A, B format 0: f16)
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// kind::tf32: tf32 A and B (both K-major), fp32 accumulator, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+    return (1u << 4)                              // D format: f32
+           | (2u << 7)                            // A format: tf32
+           | (2u << 10)                           // B format: tf32
            | (static_cast<uint32_t>(N >> 3) << 17)
            | (static_cast<uint32_t>(M >> 4) << 24);
 }
@@ -360,6 +376,12 @@ __device__ __forceinline__ uint32_t sigmoid_f16x2(float lo, float hi) {
         "fma.rn.f16x2 %0, t, c, c;\n\t}"
         : "=r"(r) : "f"(0.5f * lo), "f"(0.5f * hi));
     return r;
+}
+// x rounded to tf32 (10-bit significand, round to nearest, ties away), as an fp32 value
+__device__ __forceinline__ float tf32_round(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;

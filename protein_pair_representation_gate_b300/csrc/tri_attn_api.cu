@@ -58,15 +58,19 @@ bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) %
 Workspace layout_for(const tri_attn_ctx* c, int I) {
     const tri_attn_config& g = c->cfg;
     if (c->path == TRI_ATTN_PATH_SM103) return sm103_layout(I, g.key_chunks);
+    if (c->path == TRI_ATTN_PATH_SM103_TF32) return sm103_tf32_layout(I, g.key_chunks);
     return simt_layout(I, g.c_z, g.heads, g.head_dim, g.key_chunks);
 }
+
+// The CUDA-core kernels run every fp32-storage dtype in fp32 arithmetic.
+int simt_dtype(int dtype) { return dtype == TRI_ATTN_BF16 ? TRI_ATTN_BF16 : TRI_ATTN_F32; }
 
 bool config_ok(const tri_attn_config* g) {
     if (g->c_z < 1 || g->c_z > 256) return false;
     if (g->heads < 1 || g->heads > 16) return false;
     if (g->head_dim < 1 || g->head_dim > 64 || g->heads * g->head_dim > 256) return false;
     if (g->I_max < 1 || g->I_max > 16384) return false;
-    if (g->dtype != TRI_ATTN_F32 && g->dtype != TRI_ATTN_BF16) return false;
+    if (g->dtype != TRI_ATTN_F32 && g->dtype != TRI_ATTN_BF16 && g->dtype != TRI_ATTN_TF32) return false;
     if (!(g->ln_eps > 0.f) || g->ln_eps > 1.f) return false;
     if (g->key_chunks < 1 || g->key_chunks > 64) return false;
     return true;
@@ -94,8 +98,9 @@ tri_attn_status tri_attn_create(const tri_attn_config* cfg, tri_attn_ctx** out) 
     if (!cfg || !out) return TRI_ATTN_EINVAL;
     if (!config_ok(cfg)) return TRI_ATTN_EINVAL;
     const bool sm103 = !cfg->force_simt && sm103_supported(cfg->c_z, cfg->heads, cfg->head_dim, cfg->dtype);
+    const bool tf32 = !cfg->force_simt && sm103_tf32_supported(cfg->c_z, cfg->heads, cfg->head_dim, cfg->dtype);
     const int d = cfg->head_dim;
-    if (!sm103 && d != 8 && d != 16 && d != 32 && d != 64) return TRI_ATTN_EUNSUPPORTED;
+    if (!sm103 && !tf32 && d != 8 && d != 16 && d != 32 && d != 64) return TRI_ATTN_EUNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TRI_ATTN_ECUDA;
     int major = 0, minor = 0;
@@ -103,12 +108,12 @@ tri_attn_status tri_attn_create(const tri_attn_config* cfg, tri_attn_ctx** out) 
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return TRI_ATTN_ECUDA;
     const bool is_sm103 = major == 10 && minor == 3;                  // kernels are built for sm_103a only
-    if (sm103 && !is_sm103) return TRI_ATTN_EUNSUPPORTED;
+    if ((sm103 || tf32) && !is_sm103) return TRI_ATTN_EUNSUPPORTED;
     tri_attn_ctx* c = new (std::nothrow) tri_attn_ctx();
     if (!c) return TRI_ATTN_ENOMEM;
     c->cfg = *cfg;
     c->device = dev;
-    c->path = sm103 ? TRI_ATTN_PATH_SM103 : TRI_ATTN_PATH_SIMT;
+    c->path = sm103 ? TRI_ATTN_PATH_SM103 : tf32 ? TRI_ATTN_PATH_SM103_TF32 : TRI_ATTN_PATH_SIMT;
     c->msa_sm103 = is_sm103 && !cfg->force_simt &&
                    sm103_msa_supported(kMsaCm, cfg->c_z, cfg->heads, cfg->head_dim, cfg->dtype);
     if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess ||
@@ -159,7 +164,7 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* c, int node, int I, const void
         if (p && !aligned(p, 16)) return TRI_ATTN_EINVAL;
     const Workspace lay = layout_for(c, I);
     if (workspace_bytes < lay.total) return TRI_ATTN_ENOMEM;
-    const size_t esz = g.dtype == TRI_ATTN_F32 ? 4 : 2;
+    const size_t esz = g.dtype == TRI_ATTN_BF16 ? 2 : 4;
     const size_t pair_bytes = (size_t)I * I * g.c_z * esz;
     const bool residual = opt && opt->residual;
     const bool in_place = residual && out == Z;          // the one overlap allowed: Z += update
@@ -195,7 +200,9 @@ tri_attn_status tri_attn_forward_ex(tri_attn_ctx* c, int node, int I, const void
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LaunchTimer* t = c->timing ? &c->timer : nullptr;
-    cudaError_t e = c->path == TRI_ATTN_PATH_SM103 ? sm103_forward(a, s, t) : simt_forward(a, g.dtype, s, t);
+    cudaError_t e = c->path == TRI_ATTN_PATH_SM103        ? sm103_forward(a, s, t)
+                    : c->path == TRI_ATTN_PATH_SM103_TF32 ? sm103_tf32_forward(a, s, t)
+                                                          : simt_forward(a, simt_dtype(g.dtype), s, t);
     if (e != cudaSuccess) {
         fprintf(stderr, "tri_attn_forward: %s\n", cudaGetErrorString(e));
         return TRI_ATTN_ECUDA;
@@ -237,7 +244,7 @@ tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, con
     const Workspace lay = on_sm103 ? sm103_msa_layout(S, I, g.key_chunks)
                                    : simt_msa_layout(S, I, g.heads, g.head_dim, g.key_chunks);
     if (workspace_bytes < lay.total) return TRI_ATTN_ENOMEM;
-    const size_t esz = g.dtype == TRI_ATTN_F32 ? 4 : 2;
+    const size_t esz = g.dtype == TRI_ATTN_BF16 ? 2 : 4;
     const size_t msa_bytes = (size_t)S * I * c_m * esz, z_bytes = (size_t)I * I * g.c_z * esz;
     const bool in_place = residual && out == msa;        // the one overlap allowed: Ms += update
     if ((!in_place && overlaps(out, msa_bytes, msa, msa_bytes)) || overlaps(out, msa_bytes, Z, z_bytes) ||
@@ -269,7 +276,7 @@ tri_attn_status tri_attn_msa_forward(tri_attn_ctx* c, int S, int I, int c_m, con
     a.status = c->d_status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     LaunchTimer* t = c->timing ? &c->timer : nullptr;
-    const cudaError_t e = on_sm103 ? sm103_msa_forward(a, s, t) : simt_msa_forward(a, g.dtype, s, t);
+    const cudaError_t e = on_sm103 ? sm103_msa_forward(a, s, t) : simt_msa_forward(a, simt_dtype(g.dtype), s, t);
     if (e != cudaSuccess) {
         fprintf(stderr, "tri_attn_msa_forward: %s\n", cudaGetErrorString(e));
         return TRI_ATTN_ECUDA;
@@ -293,7 +300,7 @@ tri_attn_status tri_attn_status_sync(tri_attn_ctx* c, void* stream) {
 tri_attn_status tri_attn_debug_inject(tri_attn_ctx* c, int fault) {
     if (!c) return TRI_ATTN_EINVAL;
     if (fault != TRI_ATTN_FAULT_NONE && fault != TRI_ATTN_FAULT_SKIP_STAGE) return TRI_ATTN_EINVAL;
-    if (fault != TRI_ATTN_FAULT_NONE && c->path != TRI_ATTN_PATH_SM103) return TRI_ATTN_EUNSUPPORTED;
+    if (fault != TRI_ATTN_FAULT_NONE && c->path == TRI_ATTN_PATH_SIMT) return TRI_ATTN_EUNSUPPORTED;
     c->inject = fault;
     return TRI_ATTN_OK;
 }

@@ -166,6 +166,58 @@ constexpr Workspace sm103_msa_layout(int S, int I, int key_chunks) {
 }
 cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* t);
 
+// The attention step of the sm103 triangle path (attention, gate, output
+// projection; once per key chunk) over prepared f16 intermediates in the
+// layouts the projection writes: q, k, g [I * H][I_pad][d], v^T [I * H][d][I_pad],
+// bias [H][I_pad][I_pad], W_o^T [c_z][H d].  Z (residual) and out are bf16, or
+// fp32 with f32 set.
+struct TriAttnLaunch {
+    int node = 0, I = 0, I_pad = 0, key_chunks = 1, inject = 0;
+    bool f32 = false;
+    const uint8_t* mask = nullptr;
+    const uint8_t* pair_mask = nullptr;
+    const void* Z_resid = nullptr;     // residual source, or NULL
+    void* out = nullptr;
+    __half *q = nullptr, *k = nullptr, *vt = nullptr, *g = nullptr, *bias = nullptr, *wo_t = nullptr;
+    float *bo = nullptr, *o_run = nullptr, *lse_run = nullptr;
+    uint64_t* kbits = nullptr;         // [I][I_pad / 64 + 1] scratch (with a pair mask)
+    uint32_t* status = nullptr;
+};
+cudaError_t sm103_triangle_attention(const TriAttnLaunch& l, cudaStream_t s, LaunchTimer* t);
+
+// TF32 forward (fp32 Z, weights and out; c_z = 128, H = 4, d = 32): the LayerNorm
+// and projection on kind::tf32 tensor cores, then the attention step above with
+// f16 intermediates and fp32 out.
+bool sm103_tf32_supported(int c_z, int H, int d, int dtype);
+constexpr Workspace sm103_tf32_layout(int I, int key_chunks) {
+    Workspace w;
+    w.I = I;
+    w.I_pad = round_up(I, 256);
+    const size_t P = (size_t)I * w.I_pad;           // (line, position) slots
+    size_t off = 0;
+    auto take = [&off](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    w.wprep = take((size_t)512 * 128 * 4);          // (gamma . W)^T for q | k | v | g, tf32 values in fp32
+    w.cst = take((size_t)2 * 512 * 4);              // column sums, then offsets
+    w.wb32 = take((size_t)128 * 4 * 4 + 2 * 4 * 4); // gamma . W_b, its column sums, beta W_b
+    w.wo_t = take((size_t)128 * 128 * 2);           // W_o^T, f16
+    w.bo = take(128 * 4);
+    w.kbits = take((size_t)I * (w.I_pad / 64 + 1) * 8);
+    w.rowstat = take(P * 8);
+    w.axrow = take(P * 32);                         // two planes of 16 B per slot
+    w.q = take(P * 128 * 2);
+    w.k = take(P * 128 * 2);
+    w.v = take(P * 128 * 2);
+    w.g = take(P * 128 * 2);
+    w.bias = take((size_t)4 * w.I_pad * w.I_pad * 2);
+    if (key_chunks > 1) {
+        w.o_run = take(P * 128 * 4);
+        w.lse_run = take(P * 4 * 4);
+    }
+    w.total = off;
+    return w;
+}
+cudaError_t sm103_tf32_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* t);
+
 // Pieces of the sm103 triangle kernels the MSA path shares.
 struct MsaAttnArgs {
     int S, I, I_pad, key_chunks;
@@ -180,6 +232,10 @@ bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                  uint32_t box_rows, int swizzle_bytes, bool bf16);
 bool sm103_map3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
                       uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes);
+// fp32 tensor map of rank 1..3: dims and box innermost first, strides in bytes of
+// dims 1.. (rank - 1 of them); swizzle 128 or none.
+bool sm103_map_f32(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                   const uint32_t* box, int swizzle_bytes);
 
 // Chunk bounds shared by both paths: size = round_up(ceil(I / n), 8).
 inline int chunk_size(int I, int n) {

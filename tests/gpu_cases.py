@@ -14,13 +14,23 @@ from synth import make_inputs, with_affine_params
 F32_MAX_ABS = 1e-4
 BF16_MAX_ABS = 2e-2
 BF16_REL_L2 = 5e-3
+# TF32 mode (fp32 storage; tf32 projection operands, f16 attention operands, fp32
+# accumulation and output): the bf16 bound scaled by the ratio of the coarsest
+# rounding on each path -- tf32 truncation of the stored fp32 inputs (relative
+# error < 2^-10) against bf16 rounding of the stored inputs and the output
+# (< 2^-9) -- i.e. halved.
+TF32_MAX_ABS = BF16_MAX_ABS / 2
+TF32_REL_L2 = BF16_REL_L2 / 2
 
 
 @functools.lru_cache(maxsize=4)
-def inputs(name: str, I: int | None = None, n_pad: int | None = None, affine: bool = False):
+def inputs(name: str, I: int | None = None, n_pad: int | None = None, affine: bool = False, f32: bool = False):
+    """Seeded inputs of a workload; f32=True stores them in fp32 (the TF32 mode's storage)."""
     from dataclasses import replace
     from synth.workloads import WORKLOADS
     wl = WORKLOADS[name]
+    if f32:
+        wl = replace(wl, dtype="f32")
     if I is not None:
         wl = replace(wl, I=I, n_pad=min(wl.n_pad if n_pad is None else n_pad, I))
     elif n_pad is not None:
@@ -30,28 +40,29 @@ def inputs(name: str, I: int | None = None, n_pad: int | None = None, affine: bo
 
 
 @functools.lru_cache(maxsize=2)
-def oracle_state(name, I=None, n_pad=None, affine=False):
-    inp = inputs(name, I, n_pad, affine)
+def oracle_state(name, I=None, n_pad=None, affine=False, f32=False):
+    inp = inputs(name, I, n_pad, affine, f32)
     a = inp.oracle_args()
     return a, pair_bias(a["Z"], a["ln_gamma"], a["ln_beta"], a["w_b"])
 
 
-def oracle_out(name, node, lines=None, I=None, n_pad=None, key_chunks=1, affine=False):
-    a, bias = oracle_state(name, I, n_pad, affine)
+def oracle_out(name, node, lines=None, I=None, n_pad=None, key_chunks=1, affine=False, f32=False):
+    a, bias = oracle_state(name, I, n_pad, affine, f32)
     return triangle_attention(node, a["Z"], a["mask"], a, lines=lines, key_chunks=key_chunks, bias=bias)
 
 
 def run_library(name, nodes=("start", "end"), I=None, n_pad=None, key_chunks=1, force_simt=False, repeat=1,
-                affine=False):
+                affine=False, dtype=None):
+    """dtype "tf32" runs the fp32-stored inputs in the TF32 mode."""
     """Outputs of tri_attn_forward (through the C-ABI) as float64 numpy arrays, per node."""
     import torch
     import protein_pair_representation_gate_b300 as pkg
     from synth.device import inputs_to_device
 
-    inp = inputs(name, I, n_pad, affine)
+    inp = inputs(name, I, n_pad, affine, dtype == "tf32")
     wl = inp.workload
     t = inputs_to_device(inp, "cuda")
-    op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=key_chunks,
+    op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, dtype or wl.dtype, key_chunks=key_chunks,
                                force_simt=force_simt)
     res = {}
     for node in nodes:
@@ -86,6 +97,9 @@ def assert_close(got, want, dtype, what=""):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     if dtype == "f32":
         assert max_abs <= F32_MAX_ABS, f"{what}: max abs {max_abs:.3e} > {F32_MAX_ABS}"
+    elif dtype == "tf32":
+        assert max_abs <= TF32_MAX_ABS and rel <= TF32_REL_L2, \
+            f"{what}: max abs {max_abs:.3e} (<= {TF32_MAX_ABS}), rel L2 {rel:.3e} (<= {TF32_REL_L2})"
     else:
         assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2, \
             f"{what}: max abs {max_abs:.3e} (<= {BF16_MAX_ABS}), rel L2 {rel:.3e} (<= {BF16_REL_L2})"

@@ -15,16 +15,17 @@ def _pair_mask(I, seed=3, p_valid=0.8):
     return rng.random((I, I)) < p_valid
 
 
-def _run(name, I, n_pad, pm, nodes=NODES, key_chunks=1, force_simt=False, residual=False, in_place=False):
+def _run(name, I, n_pad, pm, nodes=NODES, key_chunks=1, force_simt=False, residual=False, in_place=False,
+         dtype=None):
     import torch
     import protein_pair_representation_gate_b300 as pkg
     from synth.device import inputs_to_device
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    inp = inputs(name, I, n_pad)
+    inp = inputs(name, I, n_pad, False, dtype == "tf32")
     wl = inp.workload
     t = inputs_to_device(inp, "cuda")
-    op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=key_chunks,
+    op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, dtype or wl.dtype, key_chunks=key_chunks,
                                force_simt=force_simt)
     dpm = torch.from_numpy(pm.astype(np.uint8)).cuda() if pm is not None else None
     res = {}
@@ -37,11 +38,11 @@ def _run(name, I, n_pad, pm, nodes=NODES, key_chunks=1, force_simt=False, residu
             out = op(node, t["Z"], t, mask=t["mask"], pair_mask=dpm, residual=residual)
         assert op.ctx.status_sync() == 0
         res[node] = out.float().cpu().numpy().astype(np.float64)
-    return res, wl.dtype
+    return res, dtype or wl.dtype
 
 
-def _want(name, node, I, n_pad, pm, key_chunks=1, residual=False):
-    a, bias = oracle_state(name, I, n_pad)
+def _want(name, node, I, n_pad, pm, key_chunks=1, residual=False, f32=False):
+    a, bias = oracle_state(name, I, n_pad, False, f32)
     return triangle_attention(node, a["Z"], a["mask"], a, key_chunks=key_chunks, bias=bias, pair_mask=pm,
                               residual=residual)
 
