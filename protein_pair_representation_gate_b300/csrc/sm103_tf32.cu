@@ -17,7 +17,7 @@
 //   sm103_tf32_prep   gamma-folded projection weights rounded to tf32 (q columns
 //                     times log2(e)/sqrt(d)), their column sums and offsets
 //                     (beta W, + b_g for the gate), gamma-folded W_b, W_o^T (f16).
-//   sm103_tf32_stats  one warp per 4 (line, position) slots in the node's
+//   sm103_tf32_stats  four threads per (line, position) slot in the node's
 //                     orientation: LayerNorm statistics of the fp32 pair vector,
 //                     the slot's row of the projection's LayerNorm K-step (tf32
 //                     hi / lo parts of -mu and 1/rstd), and the pair bias of the
@@ -130,79 +130,73 @@ __global__ void __launch_bounds__(128) sm103_tf32_prep(Tf32PrepArgs a) {
 // LayerNorm statistics, the LayerNorm K-step rows, and the pair bias
 // =====================================================================================
 // Slot (L, x): position x of line L; its pair vector is Z[L, x] (starting node) or
-// Z[x, L] (ending node).  One warp per 4 consecutive slots; lane l holds channels
-// 4l .. 4l + 3 of each.  Sums are shifted by the slot's first channel.
-constexpr int kStatSlots = 4;
+// Z[x, L] (ending node).  Four threads per slot, 32 channels each (eight float4
+// loads: a warp reads 8 whole 512-byte pair vectors), partial sums combined over
+// the four threads; sums are shifted by the slot's first channel.
+constexpr int kStatThreads = 256;
+constexpr int kStatSlotsPerBlock = kStatThreads / 4;
 
-__global__ void __launch_bounds__(256) sm103_tf32_stats(const float* Z, int node, int I, int I_pad, float eps,
-                                                        const uint8_t* mask, const float* wb, float2* rowstat,
-                                                        uint4* ax0, uint4* ax1, __half* bias) {
-    __shared__ float4 swb[CZ];                    // (gamma W_b)[c][0..3]
+__global__ void __launch_bounds__(kStatThreads) sm103_tf32_stats(const float* Z, int node, int I, int I_pad, float eps,
+                                                                 const uint8_t* mask, const float* wb, float2* rowstat,
+                                                                 uint4* ax0, uint4* ax1, __half* bias) {
+    // (gamma W_b)[c][0..3], one 33-entry row per channel quarter so that the four
+    // quarters' reads fall in different banks
+    __shared__ float4 swb[4][33];
     __shared__ float sbc[2 * NH];
-    for (int i = threadIdx.x; i < CZ; i += blockDim.x) swb[i] = reinterpret_cast<const float4*>(wb)[i];
+    for (int i = threadIdx.x; i < CZ; i += blockDim.x) swb[i >> 5][i & 31] = reinterpret_cast<const float4*>(wb)[i];
     if (threadIdx.x < 2 * NH) sbc[threadIdx.x] = wb[CZ * NH + threadIdx.x];
     __syncthreads();
-    const long long slot0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kStatSlots;
-    const int lane = threadIdx.x & 31;
+    const long long slot = (long long)blockIdx.x * kStatSlotsPerBlock + (threadIdx.x >> 2);
+    const int qtr = threadIdx.x & 3;                 // channels 32 qtr .. 32 qtr + 31
     const long long n_slots = (long long)I * I_pad;
-    float4 v[kStatSlots];
-    bool live[kStatSlots];
+    const bool in = slot < n_slots;
+    const int L = in ? (int)(slot / I_pad) : 0, x = in ? (int)(slot % I_pad) : 0;
+    const bool live = in && x < I;
+    const size_t pair = node == TRI_ATTN_STARTING ? (size_t)L * I + x : (size_t)x * I + L;
+    const float4* src = reinterpret_cast<const float4*>(Z + pair * CZ) + qtr * 8;
+    float4 v[8];
 #pragma unroll
-    for (int k = 0; k < kStatSlots; ++k) {
-        const long long slot = slot0 + k;
-        const int L = (int)(slot / I_pad), x = (int)(slot % I_pad);
-        live[k] = slot < n_slots && x < I;
-        const size_t pair = node == TRI_ATTN_STARTING ? (size_t)L * I + x : (size_t)x * I + L;
-        v[k] = live[k] ? reinterpret_cast<const float4*>(Z + pair * CZ)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const float4 w4[4] = {swb[4 * lane], swb[4 * lane + 1], swb[4 * lane + 2], swb[4 * lane + 3]};
+    for (int i = 0; i < 8; ++i) v[i] = live ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float shift = __shfl_sync(0xffffffffu, v[0].x, threadIdx.x & 28);   // channel 0 of the slot
+    float sd = 0.f, sq = 0.f, d[NH] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < kStatSlots; ++k) {
-        const float z[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        const float shift = __shfl_sync(0xffffffffu, z[0], 0);
-        float sd = 0.f, sq = 0.f, d[NH] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < 8; ++i) {
+        const float z[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
+            const float4 w = swb[qtr][4 * i + e];
             const float dz = z[e] - shift;
             sd += dz;
             sq = fmaf(dz, dz, sq);
-            d[0] = fmaf(z[e], w4[e].x, d[0]);
-            d[1] = fmaf(z[e], w4[e].y, d[1]);
-            d[2] = fmaf(z[e], w4[e].z, d[2]);
-            d[3] = fmaf(z[e], w4[e].w, d[3]);
-        }
-        for (int o = 16; o; o >>= 1) {
-            sd += __shfl_xor_sync(0xffffffffu, sd, o);
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-#pragma unroll
-            for (int h = 0; h < NH; ++h) d[h] += __shfl_xor_sync(0xffffffffu, d[h], o);
-        }
-        const long long slot = slot0 + k;
-        if (slot >= n_slots) continue;             // warp-uniform
-        const int L = (int)(slot / I_pad), x = (int)(slot % I_pad);
-        const float md = sd * (1.f / CZ);
-        const float mu = live[k] ? shift + md : 0.f;
-        const float var = fmaxf(sq * (1.f / CZ) - md * md, 0.f) + eps;
-        const float rstd = live[k] ? rsqrtf(var) : 1.f;
-        if (lane == 0) {
-            rowstat[slot] = make_float2(mu, rstd);
-            const float2 m2 = split_tf32(-mu), s2 = split_tf32(live[k] ? sqrtf(var) : 1.f);
-            ax0[slot] = make_uint4(__float_as_uint(m2.x), __float_as_uint(m2.y), __float_as_uint(m2.x),
-                                   __float_as_uint(m2.y));
-            ax1[slot] = make_uint4(__float_as_uint(s2.x), __float_as_uint(s2.y), __float_as_uint(s2.x),
-                                   __float_as_uint(s2.y));
-        }
-        if (lane < NH) {
-            // pair bias of head `lane` (log2 units): rstd (z . gW_b - mu colsum) + beta W_b
-            const bool valid = live[k] && (mask == nullptr || mask[x] != 0);
-            float dh = d[0];
-#pragma unroll
-            for (int h = 1; h < NH; ++h)
-                if (lane == h) dh = d[h];
-            const float b = (rstd * (dh - mu * sbc[lane]) + sbc[NH + lane]) * kLog2e;
-            bias[((size_t)lane * I_pad + L) * I_pad + x] = __float2half_rn(valid ? b : kMaskedBias);
+            d[0] = fmaf(z[e], w.x, d[0]);
+            d[1] = fmaf(z[e], w.y, d[1]);
+            d[2] = fmaf(z[e], w.z, d[2]);
+            d[3] = fmaf(z[e], w.w, d[3]);
         }
     }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        sd += __shfl_xor_sync(0xffffffffu, sd, o);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) d[h] += __shfl_xor_sync(0xffffffffu, d[h], o);
+    }
+    if (!in) return;
+    const float md = sd * (1.f / CZ);
+    const float mu = live ? shift + md : 0.f;
+    const float var = fmaxf(sq * (1.f / CZ) - md * md, 0.f) + eps;
+    const float rstd = live ? rsqrtf(var) : 1.f;
+    if (qtr == 0) {
+        rowstat[slot] = make_float2(mu, rstd);
+        const float2 m2 = split_tf32(-mu), s2 = split_tf32(live ? sqrtf(var) : 1.f);
+        ax0[slot] = make_uint4(__float_as_uint(m2.x), __float_as_uint(m2.y), __float_as_uint(m2.x), __float_as_uint(m2.y));
+        ax1[slot] = make_uint4(__float_as_uint(s2.x), __float_as_uint(s2.y), __float_as_uint(s2.x), __float_as_uint(s2.y));
+    }
+    // pair bias of head qtr (log2 units): rstd (z . gW_b - mu colsum) + beta W_b
+    const bool valid = live && (mask == nullptr || mask[x] != 0);
+    const float dh = qtr == 0 ? d[0] : qtr == 1 ? d[1] : qtr == 2 ? d[2] : d[3];
+    const float bv = (rstd * (dh - mu * sbc[qtr]) + sbc[NH + qtr]) * kLog2e;
+    bias[((size_t)qtr * I_pad + L) * I_pad + x] = __float2half_rn(valid ? bv : kMaskedBias);
 }
 
 // =====================================================================================
@@ -501,9 +495,9 @@ cudaError_t sm103_tf32_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm
     uint4* ax0 = reinterpret_cast<uint4*>(ws + W.axrow);
     uint4* ax1 = ax0 + P;
     {
-        const long long warps = ((long long)P + kStatSlots - 1) / kStatSlots;
+        const long long blocks = ((long long)P + kStatSlotsPerBlock - 1) / kStatSlotsPerBlock;
         if (tm) tm->begin("sm103_tf32_stats", s);
-        sm103_tf32_stats<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
+        sm103_tf32_stats<<<(unsigned)blocks, kStatThreads, 0, s>>>(
             static_cast<const float*>(a.Z), a.node, I, Ip, a.eps, a.mask, f32(W.wb32),
             reinterpret_cast<float2*>(ws + W.rowstat), ax0, ax1, hf(W.bias));
         if (tm) tm->end(s);
