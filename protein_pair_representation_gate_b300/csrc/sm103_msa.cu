@@ -502,15 +502,17 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         const int wq = warp & 3, half = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16) + half * 128;
+        // this slot's operand of a tile, loaded one tile ahead and first used a tile
+        // later (a value, not a test of it, so that nothing waits on the load here)
         float rstd = 1.f;
-        bool valid = false;
-        auto fetch = [&](int t) {             // this slot's operand of tile t
+        uint32_t mbyte = 0;
+        auto fetch = [&](int t) {
             if (t >= p.n_tiles) return;
             if (MODE == 0) {
                 rstd = p.rowstat[(size_t)t * 128 + r].y;
             } else {
                 const int s = t / tpl, i = (t % tpl) * 128 + r;
-                valid = i < p.I && (p.mask == nullptr || p.mask[(size_t)s * p.I + i] != 0);
+                mbyte = i >= p.I ? 0u : p.mask == nullptr ? 1u : static_cast<uint32_t>(p.mask[(size_t)s * p.I + i]);
             }
         };
         fetch(blockIdx.y);
@@ -520,7 +522,7 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             const int ab = j & 1;
             const int s = t / tpl, i = (t % tpl) * 128 + r;
             const float cur_rstd = rstd;
-            const bool cur_valid = valid;
+            const uint32_t cur_mbyte = mbyte;
             if (!mbar_wait(acc_full + ab, (j >> 1) & 1, abort)) { ok = false; break; }
             tc_fence_after();
             uint32_t acc[2][64];
@@ -575,6 +577,7 @@ sm103_msa_gemm(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                             zr[4 * c4 + 3] = v.w;
                         }
                     }
+                    const bool cur_valid = cur_mbyte != 0;
                     uint32_t o[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {

@@ -1,11 +1,12 @@
 """Run the library on one seeded workload, for timing and profiling (no oracle).
 
     python -m protein_pair_representation_gate_b300.run_case --workload complex_2048 --I 1024 \
-        --nodes start,end --iters 2 [--key-chunks N] [--simt] [--pair-mask DENSITY] [--residual]
+        --nodes start,end --iters 2 [--key-chunks N] [--simt] [--pair-mask DENSITY] [--residual] [--tf32]
     python -m protein_pair_representation_gate_b300.run_case --workload msa_evoformer_512 [--S 512] [--I 256]
 
 Triangle workloads go through tri_attn_forward(_ex); MSA workloads through
-tri_attn_msa_forward.  --pair-mask passes a seeded random [I, I] pair mask that
+tri_attn_msa_forward.  --tf32 runs a triangle workload's seeded values stored in
+fp32 in the TF32 mode.  --pair-mask passes a seeded random [I, I] pair mask that
 admits each pair with probability DENSITY.  Prints per-kernel CUDA-event times
 of the last iteration and the attention kernels' rate in counted TFLOP/s.
 """
@@ -39,11 +40,16 @@ def run_triangle(args):
     from synth.device import inputs_to_device
     from synth.rng import uniform01
 
-    inp = make_inputs(args.workload, I=args.I)
+    from dataclasses import replace
+    from synth.workloads import WORKLOADS
+    wl0 = WORKLOADS[args.workload]
+    if args.tf32:
+        wl0 = replace(wl0, dtype="f32")
+    inp = make_inputs(wl0, I=args.I)
     wl = inp.workload
     t = inputs_to_device(inp, "cuda")
-    op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype, key_chunks=args.key_chunks,
-                               force_simt=args.simt)
+    op = pkg.TriangleAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, "tf32" if args.tf32 else wl.dtype,
+                               key_chunks=args.key_chunks, force_simt=args.simt)
     pm = None
     if args.pair_mask is not None:
         u = uniform01(wl.seed, PAIR_MASK_STREAM, 0, wl.I * wl.I).reshape(wl.I, wl.I)
@@ -60,7 +66,7 @@ def run_triangle(args):
             raise SystemExit(f"forward failed: {pkg.status_string(st)}")
         if last:
             _report(op, wl.attention_flops(), len(nodes))
-    print(f"{args.workload} I={wl.I} nodes={args.nodes} path={['simt', 'sm103'][op.path]} "
+    print(f"{args.workload} I={wl.I} nodes={args.nodes} path={['simt', 'sm103', 'sm103_tf32'][op.path]} "
           f"pair_mask={args.pair_mask} residual={args.residual} ok")
 
 
@@ -98,6 +104,7 @@ def main():
     ap.add_argument("--simt", action="store_true")
     ap.add_argument("--pair-mask", type=float, default=None, metavar="DENSITY")
     ap.add_argument("--residual", action="store_true")
+    ap.add_argument("--tf32", action="store_true", help="fp32 storage, the TF32 mode (triangle workloads)")
     args = ap.parse_args()
 
     from synth import MSA_WORKLOADS
