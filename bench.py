@@ -11,7 +11,8 @@ Inputs (Z = 1 GiB) are larger than L2, so no flush is needed between steps.
 --chained times the Evoformer's own call pattern instead: each step updates
 the pair tensor in place, Z += start(Z) then Z += end(Z), through the residual
 entry point (the same counted work; one tensor in and one out per step end to
-end).
+end).  Without it the line also carries `e2e_chained`, that pattern's
+end-to-end measurement beside the default one.
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 (the path has no cross-GPU exchange); value = all ranks' work / max time.
@@ -489,50 +490,60 @@ def main():
                 "traffic_unit": "bytes per launch (ncu at I=512, scaled by I^2)"}
 
     # End to end through the public API with host buffers (pinned): every step copies
-    # its input Z host -> device and both nodes' outputs device -> host inside the
-    # timed region.  Copies run on their own streams, double-buffered, so step i's
-    # copies overlap the kernels of steps i-1 and i+1 (as a serving loop would).
-    e2e = None
-    if not args.no_e2e:
+    # its input Z host -> device and its results device -> host inside the timed
+    # region.  Copies run on their own streams over NB rotating buffers, so step i's
+    # copies overlap the kernels of the neighbouring steps (as a serving loop would).  The step is
+    # the timed step above (start(Z) and end(Z): two results), and, reported beside it,
+    # the Evoformer's own call pattern (Z += start(Z); Z += end(Z): one result).
+    NB = 3
+
+    def measure_e2e(chain: bool):
         hz = t["Z"].cpu().pin_memory()
-        nodes = ("z",) if chained else ("start", "end")
-        hout = [{n: torch.empty(hz.shape, dtype=hz.dtype).pin_memory() for n in nodes} for _ in range(2)]
-        dz = [torch.empty_like(t["Z"]) for _ in range(2)]
-        dout = [{n: torch.empty_like(t["Z"]) for n in nodes} for _ in range(2)]
+        nodes = ("z",) if chain else ("start", "end")
+        hout = [{n: torch.empty(hz.shape, dtype=hz.dtype).pin_memory() for n in nodes} for _ in range(NB)]
+        dz = [torch.empty_like(t["Z"]) for _ in range(NB)]
+        dout = [{n: torch.empty_like(t["Z"]) for n in nodes} for _ in range(NB)] if not chain else None
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        k = max(2, args.steps // 2)
-        n_all = k + 2
+        k = max(2 * NB, args.steps)
+        n_all = k + NB
         ev = lambda: torch.cuda.Event()
         in_done = [ev() for _ in range(n_all)]
         comp_done = [ev() for _ in range(n_all)]
         out_done = [ev() for _ in range(n_all)]
 
+        def one(z, outs):
+            for node in ("start", "end"):
+                if chain:
+                    op(node, z, t, mask=t["mask"], out=z, stream=stream, residual=True)
+                else:
+                    op(node, z, t, mask=t["mask"], out=outs[node], stream=stream)
+
         def run(i0, n):
             for i in range(i0, i0 + n):
-                b = i % 2
+                b = i % NB
                 with torch.cuda.stream(s_in):
-                    if i >= 2:
-                        s_in.wait_event(comp_done[i - 2])      # dz[b] is free again
-                        if chained:
-                            s_in.wait_event(out_done[i - 2])   # ... and its result read back
+                    if i >= NB:
+                        s_in.wait_event(comp_done[i - NB])     # dz[b] is free again
+                        if chain:
+                            s_in.wait_event(out_done[i - NB])  # ... and its result read back
                     dz[b].copy_(hz, non_blocking=True)
                     in_done[i].record(s_in)
                 stream.wait_event(in_done[i])
-                if i >= 2:
-                    stream.wait_event(out_done[i - 2])          # dout[b] has been read back
-                forward_step(dz[b], dout[b], stream)
+                if i >= NB:
+                    stream.wait_event(out_done[i - NB])         # dout[b] has been read back
+                one(dz[b], None if chain else dout[b])
                 comp_done[i].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(comp_done[i])
                     for node in nodes:
-                        hout[b][node].copy_(dz[b] if chained else dout[b][node], non_blocking=True)
+                        hout[b][node].copy_(dz[b] if chain else dout[b][node], non_blocking=True)
                     out_done[i].record(s_out)
 
-        run(0, 2)                                               # warm-up
+        run(0, NB)                                              # warm-up
         barrier()
         e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_start.record(s_in)
-        run(2, k)
+        run(NB, k)
         e_end.record(s_out)
         barrier()
         ms_e2e = e_start.elapsed_time(e_end)
@@ -541,9 +552,20 @@ def main():
             raise RuntimeError(f"end-to-end run failed: {pkg.status_string(st)}")
         ms_e2e = max_over_ranks(ms_e2e, pg, dev)
         nb = hz.numel() * hz.element_size()
-        e2e = {"value": job_tflops(flops_step, k, world, ms_e2e), "unit": UNIT,
+        res = {"value": job_tflops(flops_step, k, world, ms_e2e), "unit": UNIT,
                "h2d_bytes_per_step": nb, "d2h_bytes_per_step": len(nodes) * nb, "ms_per_step": ms_e2e / k,
-               "copies": "pinned host buffers, own streams, double-buffered across steps"}
+               "step": ("Z += start(Z); Z += end(Z), in place (residual)" if chain
+                        else "start(Z) and end(Z), update only"),
+               "copies": f"pinned host buffers, own streams, {NB} buffers rotating across steps"}
+        del hz, hout, dz, dout
+        torch.cuda.empty_cache()
+        return res
+
+    e2e = e2e_chained = None
+    if not args.no_e2e:
+        e2e = measure_e2e(chained)
+        if not chained:
+            e2e_chained = measure_e2e(True)
 
     secondary = None
     if not args.no_secondary:
@@ -562,11 +584,12 @@ def main():
                 "config": {"workload": f"{args.workload}: I={wl.I}, c_z={wl.c_z}, H={wl.heads}, d={wl.head_dim}, "
                                        "starting + ending node per step",
                            "I": wl.I, "c_z": wl.c_z, "heads": wl.heads, "head_dim": wl.head_dim,
-                           "path": ["simt", "sm103"][op.path], "l2": "inputs larger than L2 (Z = 1 GiB); no flush",
+                           "path": ["simt", "sm103", "sm103_tf32"][op.path], "l2": "inputs larger than L2 (Z = 1 GiB); no flush",
                            "step": ("Z += start(Z); Z += end(Z), in place (residual)" if chained
                                     else "start(Z) and end(Z), update only"),
                            "parallelism": f"replicas x{world}"},
                 "frac_of_peak": value / peak, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "e2e_chained": e2e_chained,
                 "gpu_launches": launches, "clocks": clocks, "secondary": secondary,
                 "kernels_ms": {k: sum(v) / len(v) for k, v in kernel_ms.items()}}
         print(json.dumps(line), flush=True)
