@@ -75,3 +75,48 @@ def test_tf32_other_shape_runs_fp32_cuda_cores():
     assert res["path"] == pkg.PATH_SIMT
     for node in NODES:
         assert_close(res[node], oracle_out("tiny_f32", node, f32=True), "f32", f"tf32 fallback {node}")
+
+
+def test_tf32_path_selection_and_timeout_recovery():
+    """Path selection for the TF32 dtype, and the bounded-wait failure path on it:
+    one block's producer skips a stage load, the launch ends with ETIMEOUT, and
+    the next forward on the same context is correct."""
+    import torch
+    from protein_pair_representation_gate_b300 import _binding as B
+    from synth.device import inputs_to_device
+    from tests.gpu_cases import inputs
+    assert B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "tf32")).path == B.PATH_SM103_TF32
+    assert B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "tf32", force_simt=True)).path == B.PATH_SIMT
+    assert B.TriAttn(B.TriAttnConfig(64, 2, 16, 64, "tf32")).path == B.PATH_SIMT
+    t = inputs_to_device(inputs("evoformer_256", 64, None, False, True), "cuda")
+    ctx = B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "tf32"))
+    ws = torch.empty(ctx.workspace_bytes(64), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(t["Z"])
+    assert ctx.debug_inject(B.FAULT_SKIP_STAGE) == B.OK
+    assert ctx.forward_status(0, 64, t["Z"], t["mask"], t, ws, out) == B.OK
+    assert ctx.status_sync() == B.ETIMEOUT
+    ctx.forward(0, 64, t["Z"], t["mask"], t, ws, out)
+    assert ctx.status_sync() == B.OK
+    got = out.cpu().numpy().astype(np.float64)
+    assert_close(got, oracle_out("evoformer_256", "start", I=64, f32=True), "tf32", "tf32 after recovery")
+
+
+def test_tf32_large_layernorm_scale_is_reported():
+    """The TF32 mode keeps f16 attention operands: a LayerNorm scale far beyond a
+    trained model's pushes them out of range, which the status word reports
+    (never silent NaN); the context works again at the normal scale."""
+    import torch
+    from protein_pair_representation_gate_b300 import _binding as B
+    from synth.device import inputs_to_device
+    from tests.gpu_cases import inputs
+    t = inputs_to_device(inputs("evoformer_256", 64, None, False, True), "cuda")
+    ctx = B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "tf32"))
+    ws = torch.empty(ctx.workspace_bytes(64), dtype=torch.uint8, device="cuda")
+    w = dict(t)
+    w["ln_gamma"] = t["ln_gamma"] * 1e5
+    out = torch.full_like(t["Z"], float("nan"))
+    ctx.forward("start", 64, t["Z"], None, w, ws, out)
+    assert ctx.status_sync() == B.ERANGE
+    ctx.forward("start", 64, t["Z"], None, t, ws, out)
+    assert ctx.status_sync() == B.OK
+    assert bool(torch.isfinite(out).all())

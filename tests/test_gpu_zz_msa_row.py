@@ -107,3 +107,27 @@ def test_msa_full_size_sampled_rows():
     assert_close(got[rows], _want(inp, rows=rows), "bf16", "msa full size")
     assert np.all(got[S - inp.workload.pad_rows:] == 0.0)
     assert np.all(got[inp.msa_mask == 0] == 0.0)
+
+
+def test_msa_large_layernorm_scale_is_reported():
+    """The tensor-core MSA path keeps f16 intermediates: an MSA LayerNorm scale far
+    beyond a trained model's pushes q, k, v out of range, which the status word
+    reports (never silent NaN); the context works again at the normal scale."""
+    import torch
+    import protein_pair_representation_gate_b300 as pkg
+    from synth import make_msa_inputs
+    from synth.device import msa_inputs_to_device
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    inp = make_msa_inputs("msa_evoformer_512", S=4, I=72)
+    wl = inp.workload
+    t = msa_inputs_to_device(inp, "cuda")
+    op = pkg.MSARowAttention(wl.c_z, wl.heads, wl.head_dim, wl.I, wl.dtype)
+    assert op.path(wl.c_m) == pkg.PATH_SM103
+    w = dict(t)
+    w["ln_m_gamma"] = t["ln_m_gamma"] * 1e5
+    op(t["Ms"], t["Z"], w, msa_mask=t["msa_mask"])
+    assert op.ctx.status_sync() == pkg._binding.ERANGE
+    out = op(t["Ms"], t["Z"], t, msa_mask=t["msa_mask"])
+    assert op.ctx.status_sync() == 0
+    assert bool(torch.isfinite(out.float()).all())
