@@ -130,33 +130,33 @@ __global__ void __launch_bounds__(128) sm103_tf32_prep(Tf32PrepArgs a) {
 // LayerNorm statistics, the LayerNorm K-step rows, and the pair bias
 // =====================================================================================
 // Slot (L, x): position x of line L; its pair vector is Z[L, x] (starting node) or
-// Z[x, L] (ending node).  Four threads per slot, 32 channels each (eight float4
-// loads: a warp reads 8 whole 512-byte pair vectors), partial sums combined over
-// the four threads; sums are shifted by the slot's first channel.
+// Z[x, L] (ending node).  Four threads per slot; thread q of a slot holds the
+// 16-byte groups q, q + 4, ..., q + 28 (channels 4g .. 4g + 3 of group g), so each
+// of the eight loads of a warp reads 64 contiguous bytes of each of its 8 pair
+// vectors.  Partial sums are combined over the four threads; sums are shifted by
+// the slot's first channel.
 constexpr int kStatThreads = 256;
 constexpr int kStatSlotsPerBlock = kStatThreads / 4;
 
 __global__ void __launch_bounds__(kStatThreads) sm103_tf32_stats(const float* Z, int node, int I, int I_pad, float eps,
                                                                  const uint8_t* mask, const float* wb, float2* rowstat,
                                                                  uint4* ax0, uint4* ax1, __half* bias) {
-    // (gamma W_b)[c][0..3], one 33-entry row per channel quarter so that the four
-    // quarters' reads fall in different banks
-    __shared__ float4 swb[4][33];
+    __shared__ float4 swb[CZ];                    // (gamma W_b)[c][0..3]
     __shared__ float sbc[2 * NH];
-    for (int i = threadIdx.x; i < CZ; i += blockDim.x) swb[i >> 5][i & 31] = reinterpret_cast<const float4*>(wb)[i];
+    for (int i = threadIdx.x; i < CZ; i += blockDim.x) swb[i] = reinterpret_cast<const float4*>(wb)[i];
     if (threadIdx.x < 2 * NH) sbc[threadIdx.x] = wb[CZ * NH + threadIdx.x];
     __syncthreads();
     const long long slot = (long long)blockIdx.x * kStatSlotsPerBlock + (threadIdx.x >> 2);
-    const int qtr = threadIdx.x & 3;                 // channels 32 qtr .. 32 qtr + 31
+    const int qtr = threadIdx.x & 3;                 // 16-byte groups qtr + 4 i
     const long long n_slots = (long long)I * I_pad;
     const bool in = slot < n_slots;
     const int L = in ? (int)(slot / I_pad) : 0, x = in ? (int)(slot % I_pad) : 0;
     const bool live = in && x < I;
     const size_t pair = node == TRI_ATTN_STARTING ? (size_t)L * I + x : (size_t)x * I + L;
-    const float4* src = reinterpret_cast<const float4*>(Z + pair * CZ) + qtr * 8;
+    const float4* src = reinterpret_cast<const float4*>(Z + pair * CZ) + qtr;
     float4 v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = live ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 8; ++i) v[i] = live ? src[4 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float shift = __shfl_sync(0xffffffffu, v[0].x, threadIdx.x & 28);   // channel 0 of the slot
     float sd = 0.f, sq = 0.f, d[NH] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kStatThreads) sm103_tf32_stats(const float* Z,
         const float z[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float4 w = swb[qtr][4 * i + e];
+            const float4 w = swb[4 * (qtr + 4 * i) + e];
             const float dz = z[e] - shift;
             sd += dz;
             sq = fmaf(dz, dz, sq);
