@@ -56,8 +56,8 @@ def parse():
 # with I^2 (the per-line K / V re-reads of the line's other query tiles are L2 hits).  Valid only for
 # the attention kernel's sources it was captured with: the hash covers that kernel's section of
 # sm103_kernels.cu and the PTX helpers; any change to them reports null until the capture is repeated.
-ATTN_TRAFFIC_I512 = 270.788608e6 + 48.105472e6
-ATTN_TRAFFIC_SRC = "7f037d44da02a080"
+ATTN_TRAFFIC_I512 = 270.771968e6 + 48.138240e6
+ATTN_TRAFFIC_SRC = "ed26199871b509e0"
 
 
 def attention_source_hash() -> str:

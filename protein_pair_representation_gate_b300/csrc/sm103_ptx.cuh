@@ -116,20 +116,7 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                  ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(src))
                  : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
-                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
-                 : "memory");
-}
-// Linear bulk store of `bytes` (a multiple of 16; both addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(reinterpret_cast<uint64_t>(gdst)), "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// all but the most recent of this thread's committed bulk stores have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // this thread's committed bulk stores have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // this thread's committed bulk stores are complete
@@ -273,13 +260,6 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[64]) {
 __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
     asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
     uint32_t r;
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
@@ -347,17 +327,6 @@ __device__ __forceinline__ float f16hi(uint32_t w) {
     asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.f32.f16 %0, b;\n\t}" : "=f"(f) : "r"(w));
     return f;
 }
-// x + (f16 half of w), the half converted exactly; one mixed-precision add
-__device__ __forceinline__ float add_f16lo(uint32_t w, float x) {
-    float r;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tadd.f32.f16 %0, a, %2;\n\t}" : "=f"(r) : "r"(w), "f"(x));
-    return r;
-}
-__device__ __forceinline__ float add_f16hi(uint32_t w, float x) {
-    float r;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %1;\n\tadd.f32.f16 %0, b, %2;\n\t}" : "=f"(r) : "r"(w), "f"(x));
-    return r;
-}
 // (a0, a1) * (b0, b1) + (c0, c1), one packed f32x2 FMA
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
     asm("{\n\t.reg .b64 a, b, c, d;\n\t"
@@ -406,10 +375,6 @@ __device__ __forceinline__ uint32_t exp2_pair_f16x2(float a, float b, float negm
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// generic-proxy writes to global memory made visible to later async-proxy (TMA) reads
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
