@@ -120,3 +120,28 @@ def test_tf32_large_layernorm_scale_is_reported():
     ctx.forward("start", 64, t["Z"], None, t, ws, out)
     assert ctx.status_sync() == B.OK
     assert bool(torch.isfinite(out).all())
+
+
+@pytest.mark.slow
+def test_tf32_complex_2048_sampled():
+    """The TF32 mode on the full I = 2048 workload (the same seeded values in fp32),
+    compared on sampled lines: chain boundaries, first and last, both nodes."""
+    from tests.gpu_cases import select
+    lines = [0, 255, 256, 1023, 2047]
+    res = run_library("complex_2048", dtype="tf32")
+    for node in NODES:
+        got = select(res[node], node, lines)
+        want = oracle_out("complex_2048", node, lines=lines, f32=True)
+        assert_close(got, want, "tf32", f"tf32 complex_2048 {node} lines={lines}")
+
+
+def test_tf32_masked_768_sampled():
+    """Padded tokens and the amplified pair bias at full size in the TF32 mode."""
+    from tests.gpu_cases import select
+    lines = [0, 345, 690, 691, 767]
+    res = run_library("masked_768", dtype="tf32")
+    for node in NODES:
+        got = select(res[node], node, lines)
+        assert_close(got, oracle_out("masked_768", node, lines=lines, f32=True), "tf32",
+                     f"tf32 masked_768 {node} lines={lines}")
+        assert np.all(res[node][691:] == 0.0) and np.all(res[node][:, 691:] == 0.0)

@@ -131,3 +131,13 @@ def test_msa_large_layernorm_scale_is_reported():
     out = op(t["Ms"], t["Z"], t, msa_mask=t["msa_mask"])
     assert op.ctx.status_sync() == 0
     assert bool(torch.isfinite(out.float()).all())
+
+
+def test_msa_long_rows_sampled():
+    """Longer MSA rows on the tensor-core path: I = 600 (three 256-query blocks,
+    ten key tiles per head, a ragged tail), S = 24, rows sampled for the oracle."""
+    import protein_pair_representation_gate_b300 as pkg
+    inp, got = _run("msa_evoformer_512", S=24, I=600, want_path=pkg.PATH_SM103)
+    rows = [0, 11, 23 - inp.workload.pad_rows, 23]
+    assert_close(got[rows], _want(inp, rows=rows), "bf16", "msa I=600 sampled rows")
+    assert np.all(got[inp.msa_mask == 0] == 0.0)
