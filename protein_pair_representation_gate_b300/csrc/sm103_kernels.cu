@@ -435,19 +435,33 @@ struct AttnParams {
 // set when key w*64 + kk < I and the pair mask admits it on that line (starting
 // node: M[L, key]; ending node: M[key, L]).  One extra zero word per line lets a
 // key tile that starts off a 64-key boundary (key chunks) read two words.
-__global__ void __launch_bounds__(128) sm103_pair_keybits(const uint8_t* pm, int node, int I, int lines, int words,
+__global__ void __launch_bounds__(256) sm103_pair_keybits(const uint8_t* pm, int node, int I, int lines, int words,
                                                           uint64_t* kbits) {
-    const int idx = blockIdx.x * 128 + threadIdx.x;
-    if (idx >= lines * words) return;
-    const int L = idx / words, w = idx % words;
-    uint64_t bits = 0;
-    for (int kk = 0; kk < 64; ++kk) {
-        const int key = w * 64 + kk;
-        if (key >= I) break;
-        const uint8_t v = node == TRI_ATTN_STARTING ? pm[(size_t)L * I + key] : pm[(size_t)key * I + L];
-        if (v) bits |= 1ull << kk;
+    // one warp per (line, word): lane l tests keys w*64 + 2l and + 1, two ballots
+    // give the word's even and odd bits
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (long long)lines * words) return;   // whole warps
+    const int L = (int)(wid / words), w = (int)(wid % words);
+    auto admitted = [&](int key) -> bool {
+        if (key >= I) return false;
+        return (node == TRI_ATTN_STARTING ? pm[(size_t)L * I + key] : pm[(size_t)key * I + L]) != 0;
+    };
+    const int key = w * 64 + 2 * lane;
+    const uint32_t ev = __ballot_sync(0xffffffffu, admitted(key));
+    const uint32_t od = __ballot_sync(0xffffffffu, admitted(key + 1));
+    if (lane == 0) {
+        auto spread = [](uint32_t v) -> uint64_t {        // bit i -> bit 2i
+            uint64_t x = v;
+            x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
+            x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
+            x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
+            x = (x | (x << 2)) & 0x3333333333333333ull;
+            x = (x | (x << 1)) & 0x5555555555555555ull;
+            return x;
+        };
+        kbits[wid] = spread(ev) | (spread(od) << 1);
     }
-    kbits[idx] = bits;
 }
 
 namespace k2 {
@@ -1344,7 +1358,8 @@ cudaError_t sm103_triangle_attention(const TriAttnLaunch& l, cudaStream_t s, Lau
         kbits = l.kbits;
         const int words = Ip / 64 + 1;
         if (tm) tm->begin("sm103_pair_keybits", s);
-        sm103_pair_keybits<<<(I * words + 127) / 128, 128, 0, s>>>(l.pair_mask, l.node, I, I, words, kbits);
+        sm103_pair_keybits<<<(unsigned)(((long long)I * words * 32 + 255) / 256), 256, 0, s>>>(l.pair_mask, l.node, I,
+                                                                                           I, words, kbits);
         if (tm) tm->end(s);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -1452,7 +1467,8 @@ cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTime
         kbits = m.kbits;
         const int words = Ip / 64 + 1;
         if (tm) tm->begin("sm103_pair_keybits", s);
-        sm103_pair_keybits<<<(m.S * words + 127) / 128, 128, 0, s>>>(m.msa_mask, TRI_ATTN_STARTING, m.I, m.S, words,
+        sm103_pair_keybits<<<(unsigned)(((long long)m.S * words * 32 + 255) / 256), 256, 0, s>>>(m.msa_mask,
+                                                                                              TRI_ATTN_STARTING, m.I, m.S, words,
                                                                     kbits);
         if (tm) tm->end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

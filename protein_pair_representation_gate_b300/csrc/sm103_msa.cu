@@ -16,7 +16,8 @@
 //                    products of length 128 per pair, from a shared-memory copy
 //                    of 64 pairs), log2(e) scaled, f16; padded keys get -30000
 //                    (finite, as on the triangle path: 2^-30000 is 0 in fp32).
-//   sm103_msa_ln_stats  LayerNorm_m mean and 1/std of every (row, residue) slot.
+//   sm103_msa_ln_stats  LayerNorm_m mean and 1/std of every (row, residue) slot
+//                    (four threads per slot), and its row of the LayerNorm K-step.
 //   sm103_msa_gemm<0>  persistent tcgen05 GEMM, one 256-column group (q, k, v
 //                    or gate) per CTA with its 128 KB of weights resident in
 //                    shared memory, 128 MSA slots per tile, K = 256 in 16 MMAs of
@@ -94,57 +95,79 @@ struct MsaPrepArgs {
     float* bo;              // [256]
 };
 
-// Blocks 0..1023: projection column n; 1024..1279: row of W_o^T; 1280: the pair-bias weights.
+// Blocks 0..31: 32 projection columns each; 32..39: 32 rows of W_o^T each; 40: the
+// pair-bias weights.  The 32-column slab of W (all 256 input channels) is staged
+// in shared memory with coalesced reads; each warp then writes 4 whole K-major
+// rows (512 bytes, one 16-byte group of 8 channels per lane).
+constexpr int kPrepCols = 32;
+
 __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
-    __shared__ float red[2][8];
-    const int n = blockIdx.x, c = threadIdx.x;
-    if (n < NPROJ) {
-        const int grp = n / CH, col = n % CH;     // q | k | v | g
+    __shared__ float tile[CM][kPrepCols + 1];
+    const int blk = blockIdx.x, c = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (blk < NPROJ / kPrepCols) {
+        const int n0 = blk * kPrepCols, grp = n0 / CH, col0 = n0 % CH;   // q | k | v | g
         const __nv_bfloat16* W = grp == 0 ? a.w_q : grp == 1 ? a.w_k : grp == 2 ? a.w_v : a.w_g;
         const float sc = grp == 0 ? kLog2e * rsqrtf((float)HD) : 1.f;   // q carries log2(e) / sqrt(d)
-        const float wv = __bfloat162float(W[c * CH + col]) * sc;
-        const __nv_bfloat16 r = __float2bfloat16_rn(a.gm[c] * wv);
-        a.wprep[(size_t)n * CM + c] = r;
-        float wr = __bfloat162float(r), bw = a.bm[c] * wv;
-        for (int o = 16; o; o >>= 1) {
-            wr += __shfl_xor_sync(0xffffffffu, wr, o);
-            bw += __shfl_xor_sync(0xffffffffu, bw, o);
-        }
-        if ((c & 31) == 0) {
-            red[0][c >> 5] = wr;
-            red[1][c >> 5] = bw;
-        }
+        for (int cc = warp; cc < CM; cc += 8) tile[cc][lane] = __bfloat162float(W[cc * CH + col0 + lane]) * sc;
         __syncthreads();
-        if (c == 0) {
-            float cs = 0.f, b = 0.f;
-            for (int i = 0; i < 8; ++i) {
-                cs += red[0][i];
-                b += red[1][i];
+        for (int jj = 0; jj < kPrepCols / 8; ++jj) {
+            const int j = warp * (kPrepCols / 8) + jj, n = n0 + j;
+            uint32_t pk[4];
+            float wr = 0.f, bw = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const int cc = lane * 8 + e;
+                const float w0 = tile[cc][j], w1 = tile[cc + 1][j];
+                const __nv_bfloat16 r0 = __float2bfloat16_rn(a.gm[cc] * w0), r1 = __float2bfloat16_rn(a.gm[cc + 1] * w1);
+                pk[e >> 1] = static_cast<uint32_t>(__bfloat16_as_ushort(r0)) |
+                             (static_cast<uint32_t>(__bfloat16_as_ushort(r1)) << 16);
+                wr += __bfloat162float(r0) + __bfloat162float(r1);
+                bw = fmaf(a.bm[cc], w0, fmaf(a.bm[cc + 1], w1, bw));
             }
-            a.cst[n] = cs;
-            a.cst[NPROJ + n] = b + (grp == 3 ? a.b_g[col] : 0.f);
+            reinterpret_cast<uint4*>(a.wprep + (size_t)n * CM)[lane] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int o = 16; o; o >>= 1) {
+                wr += __shfl_xor_sync(0xffffffffu, wr, o);
+                bw += __shfl_xor_sync(0xffffffffu, bw, o);
+            }
+            if (lane == 0) {
+                a.cst[n] = wr;
+                a.cst[NPROJ + n] = bw + (grp == 3 ? a.b_g[col0 + j] : 0.f);
+            }
         }
-    } else if (n < NPROJ + CM) {
-        const int row = n - NPROJ;                // output channel of W_o
-        a.wo_t[row * CH + c] = __float2half_rn(__bfloat162float(a.w_o[(size_t)c * CM + row]));
-        if (c == 0) a.bo[row] = a.b_o ? a.b_o[row] : 0.f;
+    } else if (blk < NPROJ / kPrepCols + CM / kPrepCols) {
+        const int row0 = (blk - NPROJ / kPrepCols) * kPrepCols;   // output channels of W_o
+        for (int cc = warp; cc < CH; cc += 8) tile[cc][lane] = __bfloat162float(a.w_o[(size_t)cc * CM + row0 + lane]);
+        __syncthreads();
+        for (int jj = 0; jj < kPrepCols / 8; ++jj) {
+            const int j = warp * (kPrepCols / 8) + jj, row = row0 + j;
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) pk[e >> 1] = pack_f16(tile[lane * 8 + e][j], tile[lane * 8 + e + 1][j]);
+            reinterpret_cast<uint4*>(a.wo_t + (size_t)row * CH)[lane] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if (lane == 0) a.bo[row] = a.b_o ? a.b_o[row] : 0.f;
+        }
     } else {
-        // gamma_z . W_b [128][8], its column sums and beta_z W_b
+        // gamma_z . W_b [128][8], its column sums and beta_z W_b: thread t owns head
+        // t % 8 over channels t / 8 + 32 k, then a reduction over the 32 threads of a head
         float* bcs = a.wb + CZ * HM;
         float* bbw = bcs + HM;
-        for (int i = c; i < CZ * HM; i += blockDim.x) {
-            const int cc = i / HM;
-            a.wb[i] = a.gz[cc] * __bfloat162float(a.w_b[i]);
+        const int h = c & (HM - 1);
+        float cs = 0.f, b = 0.f;
+        for (int cc = c >> 3; cc < CZ; cc += 32) {
+            const float wv = __bfloat162float(a.w_b[cc * HM + h]);
+            const float g = a.gz[cc] * wv;
+            a.wb[cc * HM + h] = g;
+            cs += g;
+            b = fmaf(a.bz[cc], wv, b);
         }
+        tile[c >> 3][h] = cs;                      // [32 partials][8 heads], twice
+        tile[32 + (c >> 3)][h] = b;
         __syncthreads();
-        if (c < HM) {
-            float cs = 0.f, b = 0.f;
-            for (int cc = 0; cc < CZ; ++cc) {
-                cs += a.wb[cc * HM + c];
-                b += a.bz[cc] * __bfloat162float(a.w_b[cc * HM + c]);
-            }
-            bcs[c] = cs;
-            bbw[c] = b;
+        if (c < 2 * HM) {
+            const int hh = c & (HM - 1), off = c < HM ? 0 : 32;
+            float t = 0.f;
+            for (int k = 0; k < 32; ++k) t += tile[off + k][hh];
+            (c < HM ? bcs : bbw)[hh] = t;
         }
     }
 }
@@ -232,52 +255,53 @@ __global__ void __launch_bounds__(256) sm103_msa_bias(const __nv_bfloat16* Z, in
 // =====================================================================================
 // LayerNorm_m statistics of every (row, residue) slot: rowstat[s * I_pad + i] = (mu, rstd)
 // =====================================================================================
-// One warp per 4 consecutive slots (2 KB of Ms, its four 16-byte loads a lane issued
-// together); lane l holds channels 8l .. 8l+7 of each.  Sums are shifted by the
-// slot's first channel.  Padded residues (i >= I) get (0, 1), which makes their
-// projections the plain offsets (finite; they are never attended to).
-constexpr int kStatSlots = 4;
+// Four threads per slot; thread q of a slot holds the 16-byte groups q, q + 4, ...,
+// q + 28 of its 512-byte row (eight bf16 channels each), so each of the eight
+// loads of a warp reads 64 contiguous bytes of each of its 8 slots.  Sums are
+// shifted by the slot's first channel and combined over the four threads.
+// Padded residues (i >= I) get (0, 1) and the K-step row of (mu, sd) = (0, 1),
+// which makes their projections the plain offsets (finite; never attended to).
+constexpr int kStatThreads = 256;
+constexpr int kStatSlotsPerBlock = kStatThreads / 4;
 
-__global__ void __launch_bounds__(256) sm103_msa_ln_stats(const __nv_bfloat16* M, int S, int I, int I_pad, float eps,
-                                                          float2* rowstat, uint4* axrow) {
-    const long long slot0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kStatSlots;
-    const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kStatThreads) sm103_msa_ln_stats(const __nv_bfloat16* M, int S, int I, int I_pad,
+                                                                   float eps, float2* rowstat, uint4* axrow) {
+    const long long slot = (long long)blockIdx.x * kStatSlotsPerBlock + (threadIdx.x >> 2);
+    const int q = threadIdx.x & 3;
     const long long n_slots = (long long)S * I_pad;
-    uint4 v[kStatSlots];
-    bool live[kStatSlots];
+    const bool in = slot < n_slots;
+    const int s = in ? (int)(slot / I_pad) : 0, i = in ? (int)(slot % I_pad) : 0;
+    const bool live = in && i < I;
+    const uint4* src = reinterpret_cast<const uint4*>(M + ((size_t)s * I + i) * CM) + q;
+    uint4 v[8];
 #pragma unroll
-    for (int k = 0; k < kStatSlots; ++k) {
-        const long long slot = slot0 + k;
-        const int s = (int)(slot / I_pad), i = (int)(slot % I_pad);
-        live[k] = slot < n_slots && i < I;
-        v[k] = live[k] ? reinterpret_cast<const uint4*>(M + ((size_t)s * I + i) * CM)[lane] : make_uint4(0, 0, 0, 0);
-    }
+    for (int k = 0; k < 8; ++k) v[k] = live ? src[4 * k] : make_uint4(0, 0, 0, 0);
+    const float shift = __shfl_sync(0xffffffffu, bf16lo(v[0].x), threadIdx.x & 28);   // channel 0
+    float sd = 0.f, sq = 0.f;
 #pragma unroll
-    for (int k = 0; k < kStatSlots; ++k) {
-        const float shift = __shfl_sync(0xffffffffu, bf16lo(v[k].x), 0);
+    for (int k = 0; k < 8; ++k) {
         const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        float sd = 0.f, sq = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float a = bf16lo(w4[q]) - shift, b = bf16hi(w4[q]) - shift;
+        for (int e = 0; e < 4; ++e) {
+            const float a = bf16lo(w4[e]) - shift, b = bf16hi(w4[e]) - shift;
             sd += a + b;
             sq = fmaf(a, a, fmaf(b, b, sq));
         }
-        for (int o = 16; o; o >>= 1) {
-            sd += __shfl_xor_sync(0xffffffffu, sd, o);
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        }
-        if (lane == k && slot0 + k < n_slots) {
-            const float md = sd * (1.f / CM);
-            const float mu = live[k] ? shift + md : 0.f;
-            const float var = fmaxf(sq * (1.f / CM) - md * md, 0.f) + eps;
-            rowstat[slot0 + k] = make_float2(mu, live[k] ? rsqrtf(var) : 1.f);
-            // the slot's row of the projection's LayerNorm K-step: (-mu, -mu, sd, sd) as
-            // bf16 (hi, lo) pairs, sd = sqrt(var) = 1 / rstd
-            const uint32_t m2 = split_bf16(-mu), s2 = split_bf16(live[k] ? sqrtf(var) : 1.f);
-            axrow[slot0 + k] = make_uint4(m2, m2, s2, s2);
-        }
     }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        sd += __shfl_xor_sync(0xffffffffu, sd, o);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    }
+    if (!in || q != 0) return;
+    const float md = sd * (1.f / CM);
+    const float mu = live ? shift + md : 0.f;
+    const float var = fmaxf(sq * (1.f / CM) - md * md, 0.f) + eps;
+    rowstat[slot] = make_float2(mu, live ? rsqrtf(var) : 1.f);
+    // the slot's row of the projection's LayerNorm K-step: (-mu, -mu, sd, sd) as
+    // bf16 (hi, lo) pairs, sd = sqrt(var) = 1 / rstd
+    const uint32_t m2 = split_bf16(-mu), s2 = split_bf16(live ? sqrtf(var) : 1.f);
+    axrow[slot] = make_uint4(m2, m2, s2, s2);
 }
 
 // =====================================================================================
@@ -649,7 +673,7 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
                    static_cast<const __nv_bfloat16*>(a.w.w_b), static_cast<const __nv_bfloat16*>(a.w.w_o),
                    reinterpret_cast<__nv_bfloat16*>(ws + W.wprep), f32(W.cst), f32(W.wb32), hf(W.wo_t), f32(W.bo)};
     if (tm) tm->begin("sm103_msa_prep", s);
-    sm103_msa_prep<<<NPROJ + CM + 1, 256, 0, s>>>(pa);
+    sm103_msa_prep<<<NPROJ / kPrepCols + CM / kPrepCols + 1, 256, 0, s>>>(pa);
     if (tm) tm->end(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -664,9 +688,9 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
 
     // ---- LayerNorm_m statistics of every slot
     {
-        const long long warps = ((long long)S * Ip + kStatSlots - 1) / kStatSlots;
+        const long long blocks = ((long long)S * Ip + kStatSlotsPerBlock - 1) / kStatSlotsPerBlock;
         if (tm) tm->begin("sm103_msa_ln_stats", s);
-        sm103_msa_ln_stats<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.M), S, I, Ip,
+        sm103_msa_ln_stats<<<(unsigned)blocks, kStatThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(a.M), S, I, Ip,
                                                                        a.eps, reinterpret_cast<float2*>(ws + W.rowstat),
                                                                        reinterpret_cast<uint4*>(ws + W.axrow));
         if (tm) tm->end(s);

@@ -110,18 +110,30 @@ __global__ void __launch_bounds__(128) sm103_tf32_prep(Tf32PrepArgs a) {
         a.wo_t[row * CH + c] = __float2half_rn(a.w_o[(size_t)c * CZ + row]);
         if (c == 0) a.bo[row] = a.b_o ? a.b_o[row] : 0.f;
     } else {
+        // gamma . W_b [128][4], its column sums and beta W_b (thread c owns channel c;
+        // one warp reduction per head and a 4-way sum of the warps)
+        __shared__ float part[2][4][NH];
         float* bcs = a.wb + CZ * NH;
         float* bbw = bcs + NH;
-        for (int h = 0; h < NH; ++h) a.wb[c * NH + h] = a.gamma[c] * a.w_b[c * NH + h];
-        __syncthreads();
-        if (c < NH) {
-            float cs = 0.f, b = 0.f;
-            for (int cc = 0; cc < CZ; ++cc) {
-                cs += a.wb[cc * NH + c];
-                b += a.beta[cc] * a.w_b[cc * NH + c];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const float wv = a.w_b[c * NH + h];
+            float g = a.gamma[c] * wv, b = a.beta[c] * wv;
+            a.wb[c * NH + h] = g;
+            for (int o = 16; o; o >>= 1) {
+                g += __shfl_xor_sync(0xffffffffu, g, o);
+                b += __shfl_xor_sync(0xffffffffu, b, o);
             }
-            bcs[c] = cs;
-            bbw[c] = b;
+            if ((c & 31) == 0) {
+                part[0][c >> 5][h] = g;
+                part[1][c >> 5][h] = b;
+            }
+        }
+        __syncthreads();
+        if (c < 2 * NH) {
+            const int which = c / NH, h = c % NH;
+            const float t = part[which][0][h] + part[which][1][h] + part[which][2][h] + part[which][3][h];
+            (which == 0 ? bcs : bbw)[h] = t;
         }
     }
 }
