@@ -20,6 +20,7 @@ Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -38,7 +39,7 @@ UNIT = "TFLOP/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
@@ -90,27 +91,41 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons, kept for the timed region.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    The sampler starts before the warm-up (nvidia-smi takes a moment to come up) and samples every
+    50 ms with nvidia-smi's own timestamp; mark_start()/mark_end() bracket the timed region and
+    summary() keeps only the samples taken inside it.  If none fell inside (a very short region) it
+    reports all samples and says so in "window".
+    """
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -120,23 +135,39 @@ class ClockSampler:
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
-    def summary(self):
-        sm, smax, reasons = [], None, set()
+    @staticmethod
+    def parse(lines):
+        """(timestamp or None, sm MHz, max sm MHz, set of active throttle reasons) per sample line."""
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        rows = []
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
+                sm, smax = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None
+            rows.append((ts, sm, smax, {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
+        return rows
+
+    def summary(self):
+        rows = self.parse(self.lines)
+        inside = [r for r in rows
+                  if r[0] is not None and self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "whole run (no sample fell inside the timed region)"
+        sm = [r[1] for r in inside]
+        reasons = set().union(*[r[3] for r in inside]) if inside else set()
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": inside[-1][2] if inside else None,
+                "sm_min_mhz": min(sm) if sm else None,
+                "reasons": sorted(reasons), "samples": len(sm), "period_ms": self.PERIOD_MS, "window": window}
 
 
 def dist_setup(args):
@@ -447,10 +478,12 @@ def main():
     def step():
         forward_step(zw, out, stream)
 
+    clk = ClockSampler(local).__enter__()   # sampling runs from here; summary() keeps the timed region
     for _ in range(args.warmup):
         step()
     st = lib_ctx.status_sync(stream)
     if st != 0:
+        clk.__exit__(None, None, None)
         raise RuntimeError(f"warm-up failed: {pkg.status_string(st)}")
 
     # timed region: CUDA events on the launching stream, per-kernel events inside the library
@@ -459,12 +492,14 @@ def main():
     launches = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    with ClockSampler(local) as clk:
-        e0.record(stream)
-        for _ in range(args.steps):
-            forward_step(zw, out, stream)
-        e1.record(stream)
-        barrier()
+    clk.mark_start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        forward_step(zw, out, stream)
+    e1.record(stream)
+    barrier()
+    clk.mark_end()
+    clk.__exit__(None, None, None)
     for name, ms in lib_ctx.kernel_times():
         kernel_ms.setdefault(name, []).append(ms)
         launches += 1
