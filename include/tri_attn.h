@@ -313,17 +313,19 @@ tri_attn_status tri_attn_static_status(void* stream);
 
 /* Test hook for the failure path (no GPU fault is involved).
  * fault = TRI_ATTN_FAULT_SKIP_STAGE: the next tri_attn_forward of this context
- * runs its attention kernel with the first block's producer skipping one K/V
- * stage load, so that block's bounded waits run out (about 2 s), it records the
- * timeout in the status word and exits, and later blocks of the launch exit at
- * once; tri_attn_status_sync then returns TRI_ATTN_ETIMEOUT and clears the
- * word, after which the context is fully usable.  The hook applies to one
- * forward; fault = 0 clears it.  EUNSUPPORTED on the SIMT path. */
+ * runs its attention kernel with the producer of the CTA that takes the first
+ * work item skipping one K/V stage load, so that CTA's bounded waits run out
+ * (about 2 s), it records the timeout in the status word and exits (the other
+ * CTAs take the remaining work items and finish; a later launch that finds the
+ * status set exits at once); tri_attn_status_sync then returns
+ * TRI_ATTN_ETIMEOUT and clears the word, after which the context is fully
+ * usable.  The hook applies to one forward; fault = 0 clears it.
+ * EUNSUPPORTED on the SIMT path. */
 enum { TRI_ATTN_FAULT_NONE = 0, TRI_ATTN_FAULT_SKIP_STAGE = 1 };
 tri_attn_status tri_attn_debug_inject(tri_attn_ctx* ctx, int fault);
 
 /* The same test hook for tri_attn_forward_static: the next static call (in this
- * process) runs with the first block's producer skipping one stage load;
+ * process) runs with the first work item's producer skipping one stage load;
  * tri_attn_static_status then returns TRI_ATTN_ETIMEOUT.  fault = 0 clears it. */
 tri_attn_status tri_attn_static_debug_inject(int fault);
 

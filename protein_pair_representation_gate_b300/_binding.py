@@ -245,7 +245,7 @@ class TriAttn:
         return self.lib.tri_attn_status_sync(self._h, _stream_ptr(stream))
 
     def debug_inject(self, fault: int) -> int:
-        """Test hook: the next forward's attention kernel has one block whose bounded waits run out."""
+        """Test hook: in the next forward's attention kernel, the CTA that takes the first work item skips one load, so its bounded waits run out."""
         return self.lib.tri_attn_debug_inject(self._h, fault)
 
     def set_timing(self, on: bool) -> None:

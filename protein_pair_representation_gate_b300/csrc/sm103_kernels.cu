@@ -21,7 +21,8 @@
 //                   writing q (scaled by log2(e)/sqrt(d)), k and the sigmoid
 //                   gate through TMA stores, v^T, and the log2(e)-scaled pair
 //                   bias (a finite -30000 on masked keys), all in f16.
-//   sm103_attention one CTA per (line, 256 queries); two softmax warpgroups
+//   sm103_attention persistent, one CTA per SM, claiming work items (a line
+//                   and 256 queries) from a counter; two softmax warpgroups
 //                   (128 queries each), each with its own MMA-issuing warp:
 //                   S = Q K^T + Bias I (tcgen05 into TMEM; Q copied once per
 //                   head into TMEM, the staged bias tile as an A operand
@@ -418,8 +419,10 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
 // =====================================================================================
 struct AttnParams {
     int node, I, I_pad, nk, k_begin, k_end, first, last;
+    int n_xb, lines, n_items;  // work items: (256-query block, line[, head half]); item = xb + n_xb (L + lines z)
+    int* work;                 // next unclaimed work item (zero at launch)
     __half* u;                 // MSA build: gated outputs [lines][I_pad][8 x 32] (f16), written per head
-    int inject;                // test hook: block (0,0) skips the load of stage 1
+    int inject;                // test hook: the CTA holding item 0 skips the load of its stage 1
     const uint8_t* mask;
     const uint8_t* pmask;      // [I, I] pair mask over the pairs of Z, or NULL
     const uint64_t* kbits;     // [I][I_pad / 64 + 1] key-valid bits per line (with pmask), or NULL
@@ -493,9 +496,10 @@ template <bool kEx>
 struct Lay {
     static constexpr int kME = kBias + 2 * kBStages * kBiasBytes;   // E: 128 rows x 16 B, then 2 KB of zeros
     static constexpr int kIdent = kME + (kEx ? 4096 : 0);            // 64 x 64 f16 identity (SW128, K-major)
-    static constexpr int kWo = kIdent + 8192;     // W_o^T, 2 x [128 x 128 B] (SW128), loaded at block start
-    static constexpr int kBar = kWo + 32768;
-    static constexpr int kSmem = kBar + 512 + 1024;   // barriers + alignment slack
+    static constexpr int kWo = kIdent + 8192;     // W_o^T, 2 x [128 x 128 B] (SW128), loaded at CTA start
+    static constexpr int kBo = kWo + 32768;       // b_o (128 fp32)
+    static constexpr int kBar = kBo + 512;
+    static constexpr int kSmem = kBar + 1024 + 1024;  // barriers + alignment slack
     static constexpr int kLCol = kEx ? 40 : 32;   // row of V' holding ones = column of P V' holding l
     static_assert(kIdent % 1024 == 0 && kWo % 1024 == 0, "SW128 tiles need 1024-byte alignment");
     static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
@@ -507,8 +511,79 @@ __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  /
 static_assert(kBias % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 }  // namespace k2
 
+// Block-end output of one 128-row query group: the projected rows (TMEM columns
+// tOut .. tOut + 127 of this thread's lane) + b_o, masked, plus the residual, stored
+// in the node's orientation.  out_free is signalled as soon as the last TMEM columns
+// are in registers.  Kept out of line so that its registers do not shape the
+// allocation of the attention loops.
+template <bool kEx, bool kF32>
+__device__ __noinline__ void attn_store_out(int node, int I, const uint8_t* mask, const uint8_t* pmask, const void* Z,
+                                            void* out, uint32_t tOut, int L, int x, const float* sbo,
+                                            uint64_t* out_free) {
+    constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
+    const int lane = threadIdx.x & 31;
+    const size_t pair = node == TRI_ATTN_STARTING ? (size_t)L * I + x : (size_t)x * I + L;
+    const bool valid = x < I && (mask == nullptr || mask[x] != 0) && (!kEx || pmask == nullptr || pmask[pair] != 0);
+    uint4* dst = reinterpret_cast<uint4*>(out) + pair * kRow;
+    const uint4* zres = (kEx && Z) ? reinterpret_cast<const uint4*>(Z) + pair * kRow : nullptr;
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32];
+        tmem_ld32(tOut + cb * 32, v);
+        tmem_ld_wait();
+        tmem_regs_ready(v);
+        if (cb == 3) {                       // all of the output read: S(0), S(1) of the next item may go
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(out_free);
+        }
+        if constexpr (kF32) {
+            // fp32 out (and residual): 32 channels = 8 16-byte words
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float4 zv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kEx && zres && x < I) zv = *reinterpret_cast<const float4*>(zres + cb * 8 + i);
+                const int e = 4 * i;
+                const float4 r4 = make_float4(
+                    (valid ? __uint_as_float(v[e]) + sbo[cb * 32 + e] : 0.f) + zv.x,
+                    (valid ? __uint_as_float(v[e + 1]) + sbo[cb * 32 + e + 1] : 0.f) + zv.y,
+                    (valid ? __uint_as_float(v[e + 2]) + sbo[cb * 32 + e + 2] : 0.f) + zv.z,
+                    (valid ? __uint_as_float(v[e + 3]) + sbo[cb * 32 + e + 3] : 0.f) + zv.w);
+                if (x < I) *reinterpret_cast<float4*>(dst + cb * 8 + i) = r4;
+            }
+        } else {
+            uint32_t zw[16];                     // residual (this thread's own pair: read before write)
+            if constexpr (kEx) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 zv = (zres && x < I) ? zres[cb * 4 + i] : make_uint4(0, 0, 0, 0);
+                    zw[4 * i] = zv.x;
+                    zw[4 * i + 1] = zv.y;
+                    zw[4 * i + 2] = zv.z;
+                    zw[4 * i + 3] = zv.w;
+                }
+            }
+            uint32_t o[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float a0 = valid ? __uint_as_float(v[e]) + sbo[cb * 32 + e] : 0.f;
+                float a1 = valid ? __uint_as_float(v[e + 1]) + sbo[cb * 32 + e + 1] : 0.f;
+                if constexpr (kEx) {
+                    a0 += bf16lo(zw[e >> 1]);
+                    a1 += bf16hi(zw[e >> 1]);
+                }
+                o[e >> 1] = pack_bf16(a0, a1);
+            }
+            if (x < I) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+        }
+    }
+}
+
 // kMsa: the build for MSA row attention (always with kEx): a line is an MSA row,
-// a block covers heads h0 = 4 blockIdx.z .. h0+3 of 8 (q, k, v^T, g and the pair bias hold 8
+// a work item covers heads h0 .. h0+3 of 8, h0 = 0 or 4 (q, k, v^T, g and the pair bias hold 8
 // heads per line), the MSA mask arrives as the pair mask's key bits, and each
 // head's gated output goes to global memory for the separate output projection
 // (no W_o, no epilogue here).
@@ -522,30 +597,20 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     using LY = k2::Lay<kEx>;
     static_assert(kEx || !kMsa, "the MSA build is a pair-mask build");
     constexpr int NHT = kMsa ? 8 : NH;         // heads stored per line
-    const int h0 = kMsa ? static_cast<int>(blockIdx.z) * NH : 0;   // MSA build: heads h0 .. h0 + 3 of the row
     const bool fused_out = !kMsa && p.last;   // output projection and store in this kernel
     if (status_set(p.status)) return;          // an earlier wait gave up: fail fast
-    const int L = blockIdx.y;
-    const int xq0 = blockIdx.x * 256;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (p.mask != nullptr && p.mask[L] == 0) {
-        // the whole line is padding: its update is zero (with a residual: out = Z)
-        if (p.last && (!kEx || p.Z != p.out)) {
-            constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
-            const size_t sL = p.node == TRI_ATTN_STARTING ? (size_t)p.I : 1;
-            const size_t sX = p.node == TRI_ATTN_STARTING ? 1 : (size_t)p.I;
-            for (int i = threadIdx.x; i < 256 * kRow; i += blockDim.x) {
-                const int x = xq0 + i / kRow;
-                if (x < p.I) {
-                    const size_t at = (L * sL + x * sX) * kRow + i % kRow;
-                    reinterpret_cast<uint4*>(p.out)[at] =
-                        (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z)[at] : make_uint4(0, 0, 0, 0);
-                }
-            }
-        }
-        return;
-    }
+    // Persistent (one CTA per SM): the TMA producer claims work items from a global
+    // counter (each a 256-query block of one line and, in the MSA build, one head
+    // half) and posts them in a 4-slot ring in shared memory; every role takes the
+    // same item sequence from the ring and keeps running tile and item counters, so
+    // the producers load the next item's first tiles while the current item's
+    // epilogue runs, the CTA set-up (barriers, TMEM, W_o^T) is paid once, and SMs that
+    // run slower simply take fewer items.  A claim past the last item posts -1 (end).
+    auto item_x0 = [&](int item) { return (item % p.n_xb) * 256; };
+    auto item_L = [&](int item) { return (item / p.n_xb) % p.lines; };
+    auto item_h0 = [&](int item) { return kMsa ? (item / (p.n_xb * p.lines)) * NH : 0; };  // MSA: heads h0..h0+3
+    auto skip_item = [&](int item) { return p.mask != nullptr && p.mask[item_L(item)] == 0; };
 
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::kBar);
@@ -561,11 +626,26 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     uint64_t* o_ready = bars + 20;    // [2 groups][tile parity]: P V'(it) of group g done
     uint64_t* u_full = bars + 24;     // [2]
     uint64_t* o_full = bars + 26;     // [2]
+    uint64_t* out_free = bars + 4;    // [2]: the group's output rows read from TMEM (its S columns free)
+    uint64_t* it_full = bars + 64;    // [4]: work-item slot posted
+    uint64_t* it_empty = bars + 68;   // [4]: slot read by all 12 readers (2 bias cursors, 2 MMA warps, 8 softmax warps)
+    volatile int* sitem = reinterpret_cast<volatile int*>(bars + 72);   // [4] item indices
+    // bars + 80 .. + 103: one 16-byte slot per warp (the softmax warps' current item)
     uint64_t* w_full = bars + 28;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 29);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 30);
     uint64_t* b_full = bars + 32;     // [2 groups][4]: bias tile staged
     uint64_t* b_empty = bars + 40;    // [2 groups][4]: S of that tile done (bias read)
+    // the n-th item of this CTA's sequence, for a reader that has not yet taken it
+    auto take_item = [&](int n, bool& okv) -> int {
+        const int slot = n & 3;
+        okv = __all_sync(0xffffffffu, mbar_wait(it_full + slot, (n >> 2) & 1, abort));
+        if (!okv) return -1;
+        const int item = sitem[slot];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(it_empty + slot);
+        return item;
+    };
 
     // Rows 32..47 of each stage's V': a row of ones (row kLCol: gives the softmax
     // row sum as output column kLCol of P V'), the rest zero.  With kEx, rows
@@ -590,6 +670,8 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
         *reinterpret_cast<uint4*>(sm + LY::kIdent + i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    if (fused_out)
+        for (int i = threadIdx.x; i < CZ; i += blockDim.x) reinterpret_cast<float*>(sm + LY::kBo)[i] = p.bo[i];
     if (kEx && p.kbits != nullptr)             // E: 1.0 in column 0, then its columns 8..15: zeros
         for (int i = threadIdx.x; i < 4096 / 16; i += blockDim.x)
             *reinterpret_cast<uint4*>(sm + LY::kME + i * 16) = make_uint4(i < 128 ? 0x3C00u : 0u, 0u, 0u, 0u);
@@ -603,6 +685,11 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             mbar_init(q_empty + s, 2);            // one commit per MMA issuer
             mbar_init(u_full + s, 4);
             mbar_init(o_full + s, 1);
+            mbar_init(out_free + s, 4);
+        }
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(it_full + s, 1);
+            mbar_init(it_empty + s, 12);
         }
         for (int s = 0; s < k2::kStages; ++s) {
             mbar_init(kv_full + s, 1);
@@ -650,33 +737,48 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
         bool ok = true;
         int it_issued = 0, skipped = -1, q_loads = 0;   // for the drain on the abort path
-        if (leader && fused_out) {                // W_o^T for the output projection at the block end
+        if (leader && fused_out) {                // W_o^T for every item's output projection, loaded once
             prefetch_tmap(&mapWo);
             mbar_arrive_expect_tx(w_full, 32768);
             tma_load_2d(sm + LY::kWo, &mapWo, w_full, 0, 0);
             tma_load_2d(sm + LY::kWo + 16384, &mapWo, w_full, 64, 0);
         }
-        for (int h = 0, it = 0; ok && h < NH; ++h) {
+        // it: running tile count over this CTA's items (K / V' stage and phase); hq:
+        // running head count (Q buffer hq & 1; with four heads per item its phases
+        // match the per-item head index)
+        for (int n = 0, it = 0, hq = 0; ok; ++n) {
+          const int slot = n & 3;
+          ok = __all_sync(0xffffffffu, mbar_wait(it_empty + slot, ((n >> 2) & 1) ^ 1, abort));
+          if (!ok) break;
+          if (leader) {
+              const int got = atomicAdd(p.work, 1);
+              sitem[slot] = got < p.n_items ? got : -1;
+              mbar_arrive(it_full + slot);
+          }
+          __syncwarp();
+          const int item = sitem[slot];
+          if (item < 0) break;
+          if (skip_item(item)) continue;
+          const int L = item_L(item), xq0 = item_x0(item), h0 = item_h0(item);
+          for (int h = 0; ok && h < NH; ++h, ++hq) {
             const int lh = L * NHT + h0 + h;
             for (int t = 0; t < nk; ++t, ++it) {
                 const int st = it % k2::kStages;
                 if (t == 0) {
-                    const int qb = h & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qb, ((h >> 1) & 1) ^ 1, abort));
+                    const int qb = hq & 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qb, ((hq >> 1) & 1) ^ 1, abort));
                     if (!ok) break;
                     if (leader) {
                         mbar_arrive_expect_tx(q_full + qb, 16384);
                         tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
                         tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
                     }
-                    q_loads = h + 1;
+                    q_loads = hq + 1;
                 }
                 uint32_t two = 0;                 // key-valid bits of keys k0 + 2 lane, + 1 (read before the wait;
                 if (kEx && p.kbits != nullptr) {  // k0 is a multiple of 8, so both bits sit in one 32-bit word)
-                    // (lane and line re-read here: keeping the block-start values live into this
-                    // branch costs the kernel-wide register allocation a spill)
                     const int k = p.k_begin + t * k2::kKT + 2 * static_cast<int>(lane_id());
-                    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(p.kbits + (size_t)blockIdx.y * (p.I_pad / 64 + 1));
+                    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(p.kbits + (size_t)L * (p.I_pad / 64 + 1));
                     two = wrow[k >> 5] >> (k & 31);
                 }
                 ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it / k2::kStages) & 1) ^ 1, abort));
@@ -689,7 +791,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && blockIdx.x == 0 && blockIdx.y == 0;
+                const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && item == 0;
                 if (leader && !skip) {
                     const int k0 = p.k_begin + t * k2::kKT;
                     uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
@@ -701,6 +803,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 it_issued = it + 1;
                 __syncwarp();
             }
+          }
         }
         if (fused_out) {
             // the block must not end with the W_o^T copy still writing its shared
@@ -795,56 +898,73 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             tc_commit(s_full + g * 2 + (it & 1));
             tc_commit(b_empty + g * k2::kBStages + it % k2::kBStages);   // bias tile read
         };
-        // prologue: S of tiles 0 and 1.  Group 1 starts about a microsecond later, so
-        // that the two groups' exponential phases and MMA bursts interleave instead of
-        // coinciding; with separate bias rings nothing pulls them back into step.
+        // Group 1 starts about a microsecond later, so that the two groups' exponential
+        // phases and MMA bursts interleave instead of coinciding; with separate bias
+        // rings nothing pulls them back into step.
         if (g == 1) {
             __nanosleep(500);
             __nanosleep(500);
         }
-        int hn = 0, tn = 0;                           // (head, tile) of the next S to issue
-        for (int it = 0; ok && it < 2 && it < NT; ++it) {
-            ok = s_ready(it, hn, tn);
-            if (!ok) break;
-            if (leader) issue_s_step(it, hn, tn);
-            __syncwarp();
-            if (++tn == nk) { tn = 0; ++hn; }
-        }
-        // Per tile: P(it) -> P V'(it), then at once S(it+2) into the same buffer (the
-        // tensor core runs one thread's MMAs in order).  The operands of S(it+2) are
-        // checked while P(it) is still being computed, off the P -> S path.
-        for (int it = 0, tp = 0; ok && it < NT; ++it) {
-            const int nx = it + 2;
-            if (nx < NT) {
-                ok = s_ready(nx, hn, tn);
+        // it0: running tile count of this CTA's earlier items (tile it of an item is
+        // it0 + it for stages, buffers and phases; NT is a multiple of 4, so buffer and
+        // barrier parities continue across items); done: items finished
+        for (int n = 0, it0 = 0, done = 0; ok; ++n) {
+            const int item = take_item(n, ok);
+            if (!ok || item < 0) break;
+            if (skip_item(item)) continue;
+            // the output projection of the previous item left its result in this group's
+            // S columns: S(0) and S(1) wait until the softmax warps have read it
+            if (fused_out && done > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(out_free + g, (done - 1) & 1, abort));
                 if (!ok) break;
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(p_full + g * 2 + (it & 1), (it >> 1) & 1, abort));
-            if (!ok) break;
-            if (leader) {
-                tc_fence_after();
-                issue_pv(it, tp);
-                tc_commit(o_ready + g * 2 + (it & 1));
-                tc_commit(kv_empty + it % k2::kStages);   // this group is done with the K / V' stage
-                if (nx < NT) issue_s_step(nx, hn, tn);
+            // prologue: S of tiles 0 and 1
+            int hn = 0, tn = 0;                       // (head, tile) of the next S to issue
+            for (int it = 0; ok && it < 2 && it < NT; ++it) {
+                ok = s_ready(it0 + it, hn, tn);
+                if (!ok) break;
+                if (leader) issue_s_step(it0 + it, hn, tn);
+                __syncwarp();
+                if (++tn == nk) { tn = 0; ++hn; }
             }
-            __syncwarp();
-            if (nx < NT && ++tn == nk) { tn = 0; ++hn; }
-            if (++tp == nk) tp = 0;
-        }
-        if (ok && fused_out) {                        // output projection: out = u W_o
-            constexpr uint32_t idP = idesc_f16_f32(128, 128);
-            ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, abort) && mbar_wait(u_full + g, 0, abort));
-            if (ok && leader) {
-                tc_fence_after();
+            // Per tile: P(it) -> P V'(it), then at once S(it+2) into the same buffer (the
+            // tensor core runs one thread's MMAs in order).  The operands of S(it+2) are
+            // checked while P(it) is still being computed, off the P -> S path.
+            for (int it = 0, tp = 0; ok && it < NT; ++it) {
+                const int nx = it + 2, gi = it0 + it;
+                if (nx < NT) {
+                    ok = s_ready(it0 + nx, hn, tn);
+                    if (!ok) break;
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait(p_full + g * 2 + (gi & 1), (gi >> 1) & 1, abort));
+                if (!ok) break;
+                if (leader) {
+                    tc_fence_after();
+                    issue_pv(gi, tp);
+                    tc_commit(o_ready + g * 2 + (gi & 1));
+                    tc_commit(kv_empty + gi % k2::kStages);   // this group is done with the K / V' stage
+                    if (nx < NT) issue_s_step(it0 + nx, hn, tn);
+                }
+                __syncwarp();
+                if (nx < NT && ++tn == nk) { tn = 0; ++hn; }
+                if (++tp == nk) tp = 0;
+            }
+            if (ok && fused_out) {                    // output projection: out = u W_o
+                constexpr uint32_t idP = idesc_f16_f32(128, 128);
+                ok = __all_sync(0xffffffffu, mbar_wait(w_full, 0, abort) && mbar_wait(u_full + g, done & 1, abort));
+                if (ok && leader) {
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
-                           sdesc_at(tV, smem_u32(sm + LY::kWo) + (kk >> 2) * 16384 + (kk & 3) * 32), idP,
-                           kk > 0 ? 1u : 0u);
-                tc_commit(o_full + g);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + k2::colS(g, 0), tmem + k2::colU(g) + kk * 8,
+                               sdesc_at(tV, smem_u32(sm + LY::kWo) + (kk >> 2) * 16384 + (kk & 3) * 32), idP,
+                               kk > 0 ? 1u : 0u);
+                    tc_commit(o_full + g);
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            it0 += NT;
+            ++done;
         }
         if (!ok && leader) set_abort(abort, p.status, kStatusTimeoutMma);
     } else if (warp == 3) {
@@ -854,30 +974,60 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         // polling both rings so a slower group never holds the other's loads back.
         const bool leader = elect_one();
         if (leader) prefetch_tmap(&mapB);
-        int nb0 = 0, nb1 = 0;                      // next tile to load, per group
-        bool ok = true;
-        const uint64_t t0 = globaltimer();
-        while (ok && (nb0 < NT || nb1 < NT)) {
+        // Per group: state of the item it is loading for (-2: take the next item from
+        // the ring, -1: no more items), the item's first bias row, the (head, tile) of
+        // the next load, and the running count of tiles loaded (ring stage and phase).
+        int st_[2] = {-2, -2}, row0[2] = {0, 0}, hh[2] = {0, 0}, tt[2] = {0, 0}, ni[2] = {0, 0};
+        int nb0 = 0, nb1 = 0;
+        bool ok = true, idle = false;
+        uint64_t t0 = 0;                           // start of the current run of polls without progress
+        while (ok && (st_[0] != -1 || st_[1] != -1)) {
             bool progressed = false;
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
+                if (st_[g] == -2) {                // poll the ring: never block the other group's loads
+                    const int slot = ni[g] & 3;
+                    if (!__all_sync(0xffffffffu, mbar_test(it_full + slot, (ni[g] >> 2) & 1))) continue;
+                    const int item = sitem[slot];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(it_empty + slot);
+                    ++ni[g];
+                    progressed = true;
+                    if (item < 0) {
+                        st_[g] = -1;
+                    } else if (!skip_item(item)) {
+                        st_[g] = 0;
+                        row0[g] = item_h0(item) * p.I_pad + item_x0(item) + g * 128;
+                        hh[g] = 0;
+                        tt[g] = 0;
+                    }
+                }
+                if (st_[g] < 0) continue;
                 const int j = g ? nb1 : nb0;
-                if (j >= NT) continue;
                 const int bs = g * k2::kBStages + j % k2::kBStages;
                 if (!__all_sync(0xffffffffu, mbar_test(b_empty + bs, ((j / k2::kBStages) & 1) ^ 1))) continue;
                 if (leader) {
-                    const int h = j / nk, t = j - h * nk;
                     mbar_arrive_expect_tx(b_full + bs, k2::kBiasBytes);
-                    tma_load_2d(sm + k2::kBias + bs * k2::kBiasBytes, &mapB, b_full + bs, p.k_begin + t * k2::kKT,
-                                (h0 + h) * p.I_pad + xq0 + g * 128);
+                    tma_load_2d(sm + k2::kBias + bs * k2::kBiasBytes, &mapB, b_full + bs, p.k_begin + tt[g] * k2::kKT,
+                                row0[g] + hh[g] * p.I_pad);
                 }
                 __syncwarp();
                 if (g) ++nb1; else ++nb0;
+                if (++tt[g] == nk) {
+                    tt[g] = 0;
+                    if (++hh[g] == NH) st_[g] = -2;
+                }
                 progressed = true;
             }
-            if (!progressed) {
-                if (*abort || globaltimer() - t0 > kWaitTimeoutNs) ok = false;
-                else __nanosleep(64);
+            if (progressed) {
+                idle = false;
+            } else if (!idle) {
+                idle = true;
+                t0 = globaltimer();
+            } else if (*abort || globaltimer() - t0 > kWaitTimeoutNs) {
+                ok = false;
+            } else {
+                __nanosleep(160);
             }
         }
         if (!ok) {
@@ -901,22 +1051,44 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int g = (warp - 4) >> 2;            // 0: queries xq0..+127, 1: xq0+128..+255
         const int wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int x = xq0 + g * 128 + r;
+        // the current item's line, first query and first head, kept in this warp's
+        // shared-memory slot and read where they are needed (once per head), so that
+        // they hold no registers in the tile loop
+        volatile int* wslot = reinterpret_cast<volatile int*>(bars + 80) + warp * 4;
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t tO = tl + k2::colO(g), tU = tl + k2::colU(g);
+        const float* sbo = reinterpret_cast<const float*>(sm + LY::kBo);
         float m = kMfloor;                        // running max (log2 units)
         bool ok = true;
+        constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
+        // an item whose line is padding: its update is zero (with a residual: out = Z)
+        auto fill_masked = [&](int item) {
+            if (!p.last || (kEx && p.Z == p.out)) return;
+            const int Lm = item_L(item), xm0 = item_x0(item);
+            const size_t sL = p.node == TRI_ATTN_STARTING ? (size_t)p.I : 1;
+            const size_t sX = p.node == TRI_ATTN_STARTING ? 1 : (size_t)p.I;
+            for (int i = static_cast<int>(threadIdx.x) - 128; i < 256 * kRow; i += 256) {
+                const int xm = xm0 + i / kRow;
+                if (xm < p.I) {
+                    const size_t at = (Lm * sL + xm * sX) * kRow + i % kRow;
+                    reinterpret_cast<uint4*>(p.out)[at] =
+                        (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z)[at] : make_uint4(0, 0, 0, 0);
+                }
+            }
+        };
 
         // normalise head hp, merge with the running chunk state, gate into u (TMEM)
         // gate of the head being finished, loaded at the head's last tile so that its
         // global-memory latency is hidden (heads of one tile load it in finalize)
         uint4 gpre[4];
         auto load_gate = [&](int hh) {
+            const int L = wslot[0], h0 = wslot[2], x = wslot[1] + g * 128 + r;
             const uint4* gp = reinterpret_cast<const uint4*>(p.g + (((size_t)L * NHT + h0 + hh) * p.I_pad + x) * HD);
 #pragma unroll
             for (int i = 0; i < 4; ++i) gpre[i] = gp[i];
         };
         auto finalize = [&](int hp) {
+            const int L = wslot[0], h0 = wslot[2], x = wslot[1] + g * 128 + r;
             uint32_t ov[32];
             tmem_ld32(tO, ov);
             const float l = __uint_as_float(tmem_ld1(tO + LY::kLCol));
@@ -982,175 +1154,141 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             }
         };
 
-        for (int it = 0, h = 0, t = 0; it < NT; ++it, t = (t + 1 == nk) ? 0 : t + 1, h += (t == 0) ? 1 : 0) {
-            const int b = it & 1;
-            const uint32_t tS = tl + k2::colS(g, b);
-            if (nk > 1 && t == nk - 1 && p.last) load_gate(h);
-            if (!mbar_wait(s_full + g * 2 + b, (it >> 1) & 1, abort)) { ok = false; break; }
-            tc_fence_after();
-            // ---- scores of key tile it (bias already added by the tensor core)
-            float s[k2::kKT];
-            {
-                uint32_t va[32], vb[32];
-                tmem_ld32(tS, va);
-                tmem_ld32(tS + 32, vb);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = __uint_as_float(va[i]);
-                    s[32 + i] = __uint_as_float(vb[i]);
-                }
+        // Barrier parities and phases below use the tile index within the item: NT is a
+        // multiple of 4, so they equal those of the running tile count.
+        for (int n = 0, done = 0; ok; ++n) {
+            const int item = take_item(n, ok);
+            if (!ok || item < 0) break;
+            if (skip_item(item)) {
+                fill_masked(item);
+                continue;
             }
-            const int k0 = p.k_begin + t * k2::kKT;
-            if (k0 + k2::kKT > p.k_end) {                // ragged last tile of the key range
-                const int nvalid = p.k_end - k0;
-#pragma unroll
-                for (int k = 0; k < k2::kKT; ++k)
-                    if (k >= nvalid) s[k] = -INFINITY;
+            if (lane == 0) {
+                wslot[0] = item_L(item);
+                wslot[1] = item_x0(item);
+                wslot[2] = item_h0(item);
             }
-
-            // P V'(it-2) is long complete: observing it every tile keeps the o_ready
-            // phases in step for the waits on P V'(it-1) below.  The test is issued
-            // here and its result used only at the end of the tile.
-            const bool pv2_done = it < 2 || mbar_test(o_ready + g * 2 + b, ((it - 2) >> 1) & 1);
-            // Common case (the head continues): the exponentials against the running max
-            // start at once; the tile max, needed only to detect a rescale, is computed
-            // alongside them.
-            const bool fast = t != 0;
-            uint32_t pk[32];
-            if (fast) {
-                const float negm = -m;
-#pragma unroll
-                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
-            }
-            // tile max: eight independent 3-input max chains
-            float mx[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) mx[c] = max3(s[c], s[8 + c], s[16 + c]);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[24 + c], s[32 + c]);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[40 + c], s[48 + c]);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], s[56 + c]);
-            const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-            const bool need = mt > m + 8.f;              // rescale only when the max grew by > 2^8
-            const bool redo = t == 0 || __any_sync(0xffffffffu, need);
-            if (!fast || redo) {
-                if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) { ok = false; break; }
-                auto wait_prev_pv = [&]() -> bool {
-                    if (!mbar_wait(o_ready + g * 2 + (b ^ 1), ((it - 1) >> 1) & 1, abort)) return false;
-                    tc_fence_after();
-                    return true;
-                };
-                if (t == 0) {
-                    if (it > 0) {
-                        if (!wait_prev_pv()) { ok = false; break; }
-                        finalize(h - 1);
-                    }
-                    m = fmaxf(mt, kMfloor);
-                } else if (redo) {
-                    if (!wait_prev_pv()) { ok = false; break; }
-                    uint32_t ov[32];
-                    tmem_ld32(tO, ov);
-                    uint32_t lv = tmem_ld1(tO + LY::kLCol);
+            __syncwarp();
+            for (int it = 0, h = 0, t = 0; it < NT; ++it, t = (t + 1 == nk) ? 0 : t + 1, h += (t == 0) ? 1 : 0) {
+                const int b = it & 1;
+                const uint32_t tS = tl + k2::colS(g, b);
+                if (nk > 1 && t == nk - 1 && p.last) load_gate(h);
+                if (!mbar_wait(s_full + g * 2 + b, (it >> 1) & 1, abort)) { ok = false; break; }
+                tc_fence_after();
+                // ---- scores of key tile it (bias already added by the tensor core)
+                float s[k2::kKT];
+                {
+                    uint32_t va[32], vb[32];
+                    tmem_ld32(tS, va);
+                    tmem_ld32(tS + 32, vb);
                     tmem_ld_wait();
-                    const float mn = need ? mt : m;
-                    const float alpha = ex2(m - mn);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    lv = __float_as_uint(__uint_as_float(lv) * alpha);
-                    tmem_st32(tO, ov);
-                    tmem_st1(tO + LY::kLCol, lv);
-                    m = mn;
+    #pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        s[i] = __uint_as_float(va[i]);
+                        s[32 + i] = __uint_as_float(vb[i]);
+                    }
                 }
-                const float negm = -m;
-#pragma unroll
-                for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
-            } else if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) {
-                ok = false;
+                const int k0 = p.k_begin + t * k2::kKT;
+                if (k0 + k2::kKT > p.k_end) {                // ragged last tile of the key range
+                    const int nvalid = p.k_end - k0;
+    #pragma unroll
+                    for (int k = 0; k < k2::kKT; ++k)
+                        if (k >= nvalid) s[k] = -INFINITY;
+                }
+
+                // P V'(it-2) is long complete: observing it every tile keeps the o_ready
+                // phases in step for the waits on P V'(it-1) below.  The test is issued
+                // here and its result used only at the end of the tile.
+                const bool pv2_done = it < 2 || mbar_test(o_ready + g * 2 + b, ((it - 2) >> 1) & 1);
+                // Common case (the head continues): the exponentials against the running max
+                // start at once; the tile max, needed only to detect a rescale, is computed
+                // alongside them.
+                const bool fast = t != 0;
+                uint32_t pk[32];
+                if (fast) {
+                    const float negm = -m;
+    #pragma unroll
+                    for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
+                }
+                // tile max: eight independent 3-input max chains
+                float mx[8];
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) mx[c] = max3(s[c], s[8 + c], s[16 + c]);
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[24 + c], s[32 + c]);
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[40 + c], s[48 + c]);
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], s[56 + c]);
+                const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                const bool need = mt > m + 8.f;              // rescale only when the max grew by > 2^8
+                const bool redo = t == 0 || __any_sync(0xffffffffu, need);
+                if (!fast || redo) {
+                    if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) { ok = false; break; }
+                    auto wait_prev_pv = [&]() -> bool {
+                        if (!mbar_wait(o_ready + g * 2 + (b ^ 1), ((it - 1) >> 1) & 1, abort)) return false;
+                        tc_fence_after();
+                        return true;
+                    };
+                    if (t == 0) {
+                        if (it > 0) {
+                            if (!wait_prev_pv()) { ok = false; break; }
+                            finalize(h - 1);
+                        }
+                        m = fmaxf(mt, kMfloor);
+                    } else if (redo) {
+                        if (!wait_prev_pv()) { ok = false; break; }
+                        uint32_t ov[32];
+                        tmem_ld32(tO, ov);
+                        uint32_t lv = tmem_ld1(tO + LY::kLCol);
+                        tmem_ld_wait();
+                        const float mn = need ? mt : m;
+                        const float alpha = ex2(m - mn);
+    #pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        lv = __float_as_uint(__uint_as_float(lv) * alpha);
+                        tmem_st32(tO, ov);
+                        tmem_st1(tO + LY::kLCol, lv);
+                        m = mn;
+                    }
+                    const float negm = -m;
+    #pragma unroll
+                    for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
+                } else if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tmem_st32(tS, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full + g * 2 + b);
+            }
+            if (ok && NT >= 2) ok = mbar_wait(o_ready + g * 2 + (NT & 1), ((NT - 2) >> 1) & 1, abort);
+            if (ok) ok = mbar_wait(o_ready + g * 2 + ((NT - 1) & 1), ((NT - 1) >> 1) & 1, abort);
+            if (ok) {
+                tc_fence_after();
+                finalize(NH - 1);
+            }
+            if (!ok) {
+                set_abort(abort, p.status, kStatusTimeoutSoftmax);
                 break;
             }
-            tmem_st32(tS, pk);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + g * 2 + b);
-        }
-        if (ok && NT >= 2) ok = mbar_wait(o_ready + g * 2 + (NT & 1), ((NT - 2) >> 1) & 1, abort);
-        if (ok) ok = mbar_wait(o_ready + g * 2 + ((NT - 1) & 1), ((NT - 1) >> 1) & 1, abort);
-        if (ok) {
-            tc_fence_after();
-            finalize(NH - 1);
-        }
-        if (!ok) set_abort(abort, p.status, kStatusTimeoutSoftmax);
-        if (ok && fused_out) {
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(u_full + g);
-            if (mbar_wait(o_full + g, 0, abort)) {
-                tc_fence_after();
-                const size_t pair = p.node == TRI_ATTN_STARTING ? (size_t)L * p.I + x : (size_t)x * p.I + L;
-                const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0) &&
-                                   (!kEx || p.pmask == nullptr || p.pmask[pair] != 0);
-                constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
-                uint4* dst = reinterpret_cast<uint4*>(p.out) + pair * kRow;
-                const uint4* zres = (kEx && p.Z) ? reinterpret_cast<const uint4*>(p.Z) + pair * kRow : nullptr;
-                const uint32_t tOut = tl + k2::colS(g, 0);
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t v[32];
-                    tmem_ld32(tOut + cb * 32, v);
-                    tmem_ld_wait();
-                    tmem_regs_ready(v);
-                    if constexpr (kF32) {
-                        // fp32 out (and residual): 32 channels = 8 16-byte words
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float4 zv = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (kEx && zres && x < p.I) zv = *reinterpret_cast<const float4*>(zres + cb * 8 + i);
-                            const int e = 4 * i;
-                            const float4 r4 = make_float4(
-                                (valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f) + zv.x,
-                                (valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f) + zv.y,
-                                (valid ? __uint_as_float(v[e + 2]) + p.bo[cb * 32 + e + 2] : 0.f) + zv.z,
-                                (valid ? __uint_as_float(v[e + 3]) + p.bo[cb * 32 + e + 3] : 0.f) + zv.w);
-                            if (x < p.I) *reinterpret_cast<float4*>(dst + cb * 8 + i) = r4;
-                        }
-                    } else {
-                        uint32_t zw[16];                     // residual (this thread's own pair: read before write)
-                        if constexpr (kEx) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const uint4 zv = (zres && x < p.I) ? zres[cb * 4 + i] : make_uint4(0, 0, 0, 0);
-                                zw[4 * i] = zv.x;
-                                zw[4 * i + 1] = zv.y;
-                                zw[4 * i + 2] = zv.z;
-                                zw[4 * i + 3] = zv.w;
-                            }
-                        }
-                        uint32_t o[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float a0 = valid ? __uint_as_float(v[e]) + p.bo[cb * 32 + e] : 0.f;
-                            float a1 = valid ? __uint_as_float(v[e + 1]) + p.bo[cb * 32 + e + 1] : 0.f;
-                            if constexpr (kEx) {
-                                a0 += bf16lo(zw[e >> 1]);
-                                a1 += bf16hi(zw[e >> 1]);
-                            }
-                            o[e >> 1] = pack_bf16(a0, a1);
-                        }
-                        if (x < p.I) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                        }
-                    }
+            if (fused_out) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(u_full + g);
+                if (mbar_wait(o_full + g, done & 1, abort)) {
+                    tc_fence_after();
+                    attn_store_out<kEx, kF32>(p.node, p.I, p.mask, p.pmask, p.Z, p.out, tl + k2::colS(g, 0),
+                                              wslot[0], wslot[1] + g * 128 + r, sbo, out_free + g);
+                } else {
+                    set_abort(abort, p.status, kStatusTimeoutEpilogue);
+                    ok = false;
                 }
-            } else {
-                set_abort(abort, p.status, kStatusTimeoutEpilogue);
             }
+            ++done;
         }
     }
     tc_fence_before();
@@ -1320,6 +1458,7 @@ cudaError_t sm103_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm) {
     l.o_run = W.o_run ? f32(W.o_run) : nullptr;
     l.lse_run = W.lse_run ? f32(W.lse_run) : nullptr;
     l.kbits = reinterpret_cast<uint64_t*>(a.ws + W.kbits);
+    l.work = reinterpret_cast<int*>(a.ws + W.work);
     l.status = a.status;
     return sm103_triangle_attention(l, s, tm);
 }
@@ -1388,7 +1527,13 @@ cudaError_t sm103_triangle_attention(const TriAttnLaunch& l, cudaStream_t s, Lau
         ap.status = l.status;
         ap.inject = k0 == 0 ? l.inject : 0;
         ap.u = nullptr;
-        dim3 grid(Ip / 256, I);
+        ap.n_xb = Ip / 256;
+        ap.lines = I;
+        ap.n_items = ap.n_xb * I;
+        ap.work = l.work;
+        const dim3 grid(ap.n_items < num_sms() ? ap.n_items : num_sms());   // persistent: one CTA per SM
+        e = cudaMemsetAsync(l.work, 0, sizeof(int), s);
+        if (e != cudaSuccess) return e;
         const bool ex = ap.kbits != nullptr || ap.Z != nullptr;
         if (tm) tm->begin("sm103_attention", s);
         if (l.f32) {
@@ -1498,7 +1643,12 @@ cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTime
             ap.out = nullptr;
             ap.status = m.status;
             ap.inject = 0;
-            dim3 grid(Ip / 256, m.S, 8 / NH);
+            ap.n_xb = Ip / 256;
+            ap.lines = m.S;
+            ap.n_items = ap.n_xb * m.S * (8 / NH);
+            ap.work = m.work;
+            const dim3 grid(ap.n_items < num_sms() ? ap.n_items : num_sms());   // persistent: one CTA per SM
+            if ((e = cudaMemsetAsync(m.work, 0, sizeof(int), s)) != cudaSuccess) return e;
             if (tm) tm->begin("sm103_attention", s);
             sm103_attention<true, true><<<grid, k2::kThreads, k2::Lay<true>::kSmem, s>>>(mQ, mK, mV, mB, mB, ap);
             if (tm) tm->end(s);

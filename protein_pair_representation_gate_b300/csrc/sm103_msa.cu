@@ -731,7 +731,7 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
     {
         MsaAttnArgs m{S, I, Ip, a.key_chunks, hf(W.q), hf(W.k), hf(W.v), hf(W.g), hf(W.bias), hf(W.u),
                       W.o_run ? f32(W.o_run) : nullptr, W.lse_run ? f32(W.lse_run) : nullptr, a.msa_mask,
-                      reinterpret_cast<uint64_t*>(ws + W.kbits), a.status};
+                      reinterpret_cast<uint64_t*>(ws + W.kbits), a.status, reinterpret_cast<int*>(ws + W.work)};
         if ((e = sm103_msa_attention(m, s, tm)) != cudaSuccess) return e;
     }
 

@@ -572,6 +572,7 @@ cudaError_t sm103_tf32_forward(const FwdArgs& a, cudaStream_t s, LaunchTimer* tm
     l.o_run = W.o_run ? f32(W.o_run) : nullptr;
     l.lse_run = W.lse_run ? f32(W.lse_run) : nullptr;
     l.kbits = reinterpret_cast<uint64_t*>(ws + W.kbits);
+    l.work = reinterpret_cast<int*>(ws + W.work);
     l.status = a.status;
     return sm103_triangle_attention(l, s, tm);
 }

@@ -47,6 +47,7 @@ struct Workspace {
     size_t kbits = 0;                                        // [I][I_pad / 64 + 1] key-valid bits per line (sm103)
     size_t rowstat = 0;                                      // (mu, rstd) per MSA slot (sm103 MSA path)
     size_t axrow = 0;                                        // 16 B per MSA slot: its LayerNorm K-step row
+    size_t work = 0;                                         // work-item counter of the attention kernel
     size_t total = 0;
 };
 
@@ -117,6 +118,7 @@ constexpr Workspace sm103_layout(int I, int key_chunks) {
     w.bo = take(128 * 4);
     w.cst = take(256 * 4 * 4);
     w.kbits = take((size_t)I * (w.I_pad / 64 + 1) * 8);
+    w.work = take(256);
     w.q = take(P * 128 * 2);
     w.k = take(P * 128 * 2);
     w.v = take(P * 128 * 2);
@@ -149,6 +151,7 @@ constexpr Workspace sm103_msa_layout(int S, int I, int key_chunks) {
     w.wo_t = take((size_t)256 * 256 * 2);             // W_o^T, f16
     w.bo = take(256 * 4);
     w.kbits = take((size_t)S * (w.I_pad / 64 + 1) * 8);
+    w.work = take(256);
     w.rowstat = take(P * 8);
     w.axrow = take(P * 16);
     w.q = take(P * 256 * 2);
@@ -181,6 +184,7 @@ struct TriAttnLaunch {
     __half *q = nullptr, *k = nullptr, *vt = nullptr, *g = nullptr, *bias = nullptr, *wo_t = nullptr;
     float *bo = nullptr, *o_run = nullptr, *lse_run = nullptr;
     uint64_t* kbits = nullptr;         // [I][I_pad / 64 + 1] scratch (with a pair mask)
+    int* work = nullptr;               // work-item counter (zeroed before each launch)
     uint32_t* status = nullptr;
 };
 cudaError_t sm103_triangle_attention(const TriAttnLaunch& l, cudaStream_t s, LaunchTimer* t);
@@ -202,6 +206,7 @@ constexpr Workspace sm103_tf32_layout(int I, int key_chunks) {
     w.wo_t = take((size_t)128 * 128 * 2);           // W_o^T, f16
     w.bo = take(128 * 4);
     w.kbits = take((size_t)I * (w.I_pad / 64 + 1) * 8);
+    w.work = take(256);
     w.rowstat = take(P * 8);
     w.axrow = take(P * 32);                         // two planes of 16 B per slot
     w.q = take(P * 128 * 2);
@@ -226,6 +231,7 @@ struct MsaAttnArgs {
     const uint8_t* msa_mask;
     uint64_t* kbits;
     uint32_t* status;
+    int* work;                 // work-item counter (zeroed before each launch)
 };
 cudaError_t sm103_msa_attention(const MsaAttnArgs& m, cudaStream_t s, LaunchTimer* t);
 bool sm103_map2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
