@@ -511,21 +511,31 @@ __host__ __device__ constexpr uint32_t colU(int g) { return 384u + g * 64u; }  /
 static_assert(kBias % 1024 == 0 && kStageBytes % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 }  // namespace k2
 
-// Block-end output of one 128-row query group: the projected rows (TMEM columns
+// Item-end output of one 128-row query group: the projected rows (TMEM columns
 // tOut .. tOut + 127 of this thread's lane) + b_o, masked, plus the residual, stored
 // in the node's orientation.  out_free is signalled as soon as the last TMEM columns
-// are in registers.  Kept out of line so that its registers do not shape the
-// allocation of the attention loops.
+// are in registers.  The bf16 builds call it out of line (attn_store_out_call), so
+// that its registers do not shape the allocation of the attention loops; the fp32
+// build inlines it (out of line, that build's attention launch took 12.0 instead of
+// 10.7 ms at I = 2048).
+// 32-byte global store (eight 32-bit words; the address must be 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 template <bool kEx, bool kF32>
-__device__ __noinline__ void attn_store_out(int node, int I, const uint8_t* mask, const uint8_t* pmask, const void* Z,
-                                            void* out, uint32_t tOut, int L, int x, const float* sbo,
-                                            uint64_t* out_free) {
+__device__ __forceinline__ void attn_store_out(int node, int I, const uint8_t* mask, const uint8_t* pmask,
+                                               const void* Z, void* out, uint32_t tOut, int L, int x,
+                                               const float* sbo, uint64_t* out_free) {
     constexpr int kRow = CZ * (kF32 ? 4 : 2) / 16;   // 16-byte words per pair vector
     const int lane = threadIdx.x & 31;
     const size_t pair = node == TRI_ATTN_STARTING ? (size_t)L * I + x : (size_t)x * I + L;
     const bool valid = x < I && (mask == nullptr || mask[x] != 0) && (!kEx || pmask == nullptr || pmask[pair] != 0);
     uint4* dst = reinterpret_cast<uint4*>(out) + pair * kRow;
     const uint4* zres = (kEx && Z) ? reinterpret_cast<const uint4*>(Z) + pair * kRow : nullptr;
+    const bool wide = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;   // rows then start on 32 bytes
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         uint32_t v[32];
@@ -539,6 +549,7 @@ __device__ __noinline__ void attn_store_out(int node, int I, const uint8_t* mask
         }
         if constexpr (kF32) {
             // fp32 out (and residual): 32 channels = 8 16-byte words
+            uint32_t w[32];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float4 zv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -549,7 +560,20 @@ __device__ __noinline__ void attn_store_out(int node, int I, const uint8_t* mask
                     (valid ? __uint_as_float(v[e + 1]) + sbo[cb * 32 + e + 1] : 0.f) + zv.y,
                     (valid ? __uint_as_float(v[e + 2]) + sbo[cb * 32 + e + 2] : 0.f) + zv.z,
                     (valid ? __uint_as_float(v[e + 3]) + sbo[cb * 32 + e + 3] : 0.f) + zv.w);
-                if (x < I) *reinterpret_cast<float4*>(dst + cb * 8 + i) = r4;
+                w[4 * i] = __float_as_uint(r4.x);
+                w[4 * i + 1] = __float_as_uint(r4.y);
+                w[4 * i + 2] = __float_as_uint(r4.z);
+                w[4 * i + 3] = __float_as_uint(r4.w);
+            }
+            if (x < I) {
+                if (wide) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) st_global_v8(dst + cb * 8 + 2 * j, w + 8 * j);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[cb * 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
             }
         } else {
             uint32_t zw[16];                     // residual (this thread's own pair: read before write)
@@ -575,11 +599,24 @@ __device__ __noinline__ void attn_store_out(int node, int I, const uint8_t* mask
                 o[e >> 1] = pack_bf16(a0, a1);
             }
             if (x < I) {
+                if (wide) {
+                    st_global_v8(dst + cb * 4, o);
+                    st_global_v8(dst + cb * 4 + 2, o + 8);
+                } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i)
+                        dst[cb * 4 + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
             }
         }
     }
+}
+
+template <bool kEx>
+__device__ __noinline__ void attn_store_out_call(int node, int I, const uint8_t* mask, const uint8_t* pmask,
+                                                 const void* Z, void* out, uint32_t tOut, int L, int x,
+                                                 const float* sbo, uint64_t* out_free) {
+    attn_store_out<kEx, false>(node, I, mask, pmask, Z, out, tOut, L, x, sbo, out_free);
 }
 
 // kMsa: the build for MSA row attention (always with kEx): a line is an MSA row,
@@ -1145,9 +1182,10 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     }
                 }
                 if constexpr (kMsa) {
+                    // 64 bytes of the slot's 512-byte row (workspace: 256-byte aligned)
                     uint4* dst = reinterpret_cast<uint4*>(p.u + ((size_t)L * p.I_pad + x) * (NHT * HD) + (h0 + hp) * HD);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
+                    st_global_v8(dst, u);
+                    st_global_v8(dst + 2, u + 8);
                 } else {
                     tmem_st16(tU + hp * 16, u);
                 }
@@ -1281,8 +1319,12 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (lane == 0) mbar_arrive(u_full + g);
                 if (mbar_wait(o_full + g, done & 1, abort)) {
                     tc_fence_after();
-                    attn_store_out<kEx, kF32>(p.node, p.I, p.mask, p.pmask, p.Z, p.out, tl + k2::colS(g, 0),
-                                              wslot[0], wslot[1] + g * 128 + r, sbo, out_free + g);
+                    if constexpr (kF32)
+                        attn_store_out<kEx, true>(p.node, p.I, p.mask, p.pmask, p.Z, p.out, tl + k2::colS(g, 0),
+                                                  wslot[0], wslot[1] + g * 128 + r, sbo, out_free + g);
+                    else
+                        attn_store_out_call<kEx>(p.node, p.I, p.mask, p.pmask, p.Z, p.out, tl + k2::colS(g, 0),
+                                                 wslot[0], wslot[1] + g * 128 + r, sbo, out_free + g);
                 } else {
                     set_abort(abort, p.status, kStatusTimeoutEpilogue);
                     ok = false;
