@@ -57,8 +57,8 @@ def parse():
 # with I^2 (the per-line K / V re-reads of the line's other query tiles are L2 hits).  Valid only for
 # the attention kernel's sources it was captured with: the hash covers that kernel's section of
 # sm103_kernels.cu and the PTX helpers; any change to them reports null until the capture is repeated.
-ATTN_TRAFFIC_I512 = 270.874624e6 + 47.504640e6
-ATTN_TRAFFIC_SRC = "753235562b0aa630"
+ATTN_TRAFFIC_I512 = 270.830080e6 + 48.575232e6
+ATTN_TRAFFIC_SRC = "f6d1a4e5ff64319f"
 
 
 def attention_source_hash() -> str:
