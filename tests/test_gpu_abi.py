@@ -87,6 +87,44 @@ def test_timing_records_each_kernel(setup):
     assert ctx.status_sync() == B.OK
 
 
+def test_output_only_16_byte_aligned(setup):
+    """The ABI asks only for a 16-byte aligned out.  The attention epilogue writes
+    each output row in 32-byte pieces when out is 32-byte aligned and in 16-byte
+    pieces otherwise; both give the same bits (bf16 build, and the fp32-output
+    build of the TF32 mode)."""
+    torch, t, ctx, ws = setup
+    n = t["Z"].numel()
+    ref = torch.empty_like(t["Z"])
+    buf = torch.empty(n + 8, dtype=t["Z"].dtype, device="cuda")
+    off = buf[8:].view_as(t["Z"])                        # 16 bytes past a 256-byte boundary
+    assert off.data_ptr() % 32 == 16
+    for node in (0, 1):
+        ctx.forward(node, 64, t["Z"], t["mask"], t, ws, ref)
+        ctx.forward(node, 64, t["Z"], t["mask"], t, ws, off)
+        torch.cuda.synchronize()
+        assert torch.equal(ref, off), node
+    assert ctx.status_sync() == B.OK
+
+    from dataclasses import replace
+    from synth import make_inputs
+    from synth.device import inputs_to_device
+    from synth.workloads import WORKLOADS
+    t32 = inputs_to_device(make_inputs(replace(WORKLOADS["evoformer_256"], dtype="f32"), I=64), "cuda")
+    ctx32 = B.TriAttn(B.TriAttnConfig(128, 4, 32, 64, "tf32"))
+    assert ctx32.path == B.PATH_SM103_TF32
+    ws32 = torch.empty(ctx32.workspace_bytes(64), dtype=torch.uint8, device="cuda")
+    ref32 = torch.empty_like(t32["Z"])
+    buf32 = torch.empty(n + 4, dtype=t32["Z"].dtype, device="cuda")
+    off32 = buf32[4:].view_as(t32["Z"])
+    assert off32.data_ptr() % 32 == 16
+    for node in (0, 1):
+        ctx32.forward(node, 64, t32["Z"], t32["mask"], t32, ws32, ref32)
+        ctx32.forward(node, 64, t32["Z"], t32["mask"], t32, ws32, off32)
+        torch.cuda.synchronize()
+        assert torch.equal(ref32, off32), node
+    assert ctx32.status_sync() == B.OK
+
+
 def test_bounded_wait_timeout_is_reported_and_context_recovers(setup):
     """Failure path without a GPU fault: one block's producer skips a stage load,
     its bounded waits run out (~2 s), the launch finishes, status_sync reports
