@@ -58,7 +58,7 @@ def parse():
 # the attention kernel's sources it was captured with: the hash covers that kernel's section of
 # sm103_kernels.cu and the PTX helpers; any change to them reports null until the capture is repeated.
 ATTN_TRAFFIC_I512 = 270.830080e6 + 48.575232e6
-ATTN_TRAFFIC_SRC = "f6d1a4e5ff64319f"
+ATTN_TRAFFIC_SRC = "5c47bcd85aa50e7c"
 
 
 def attention_source_hash() -> str:

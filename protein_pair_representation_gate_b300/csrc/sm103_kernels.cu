@@ -784,63 +784,66 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         // running head count (Q buffer hq & 1; with four heads per item its phases
         // match the per-item head index)
         for (int n = 0, it = 0, hq = 0; ok; ++n) {
-          const int slot = n & 3;
-          ok = __all_sync(0xffffffffu, mbar_wait(it_empty + slot, ((n >> 2) & 1) ^ 1, abort));
-          if (!ok) break;
-          if (leader) {
-              const int got = atomicAdd(p.work, 1);
-              sitem[slot] = got < p.n_items ? got : -1;
-              mbar_arrive(it_full + slot);
-          }
-          __syncwarp();
-          const int item = sitem[slot];
-          if (item < 0) break;
-          if (skip_item(item)) continue;
-          const int L = item_L(item), xq0 = item_x0(item), h0 = item_h0(item);
-          for (int h = 0; ok && h < NH; ++h, ++hq) {
-            const int lh = L * NHT + h0 + h;
-            for (int t = 0; t < nk; ++t, ++it) {
-                const int st = it % k2::kStages;
-                if (t == 0) {
-                    const int qb = hq & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qb, ((hq >> 1) & 1) ^ 1, abort));
-                    if (!ok) break;
-                    if (leader) {
-                        mbar_arrive_expect_tx(q_full + qb, 16384);
-                        tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
-                        tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0 + 128);
+            const int slot = n & 3;
+            ok = __all_sync(0xffffffffu, mbar_wait(it_empty + slot, ((n >> 2) & 1) ^ 1, abort));
+            if (!ok) break;
+            if (leader) {
+                const int got = atomicAdd(p.work, 1);
+                sitem[slot] = got < p.n_items ? got : -1;
+                mbar_arrive(it_full + slot);
+            }
+            __syncwarp();
+            const int item = sitem[slot];
+            if (item < 0) break;
+            if (skip_item(item)) continue;
+            const int L = item_L(item), xq0 = item_x0(item), h0 = item_h0(item);
+            for (int h = 0; ok && h < NH; ++h, ++hq) {
+                const int lh = L * NHT + h0 + h;
+                for (int t = 0; t < nk; ++t, ++it) {
+                    const int st = it % k2::kStages;
+                    if (t == 0) {
+                        const int qb = hq & 1;
+                        ok = __all_sync(0xffffffffu, mbar_wait(q_empty + qb, ((hq >> 1) & 1) ^ 1, abort));
+                        if (!ok) break;
+                        if (leader) {
+                            mbar_arrive_expect_tx(q_full + qb, 16384);
+                            tma_load_2d(sm + k2::kQ + qb * 16384, &mapQ, q_full + qb, 0, lh * p.I_pad + xq0);
+                            tma_load_2d(sm + k2::kQ + qb * 16384 + 8192, &mapQ, q_full + qb, 0,
+                                        lh * p.I_pad + xq0 + 128);
+                        }
+                        q_loads = hq + 1;
                     }
-                    q_loads = hq + 1;
-                }
-                uint32_t two = 0;                 // key-valid bits of keys k0 + 2 lane, + 1 (read before the wait;
-                if (kEx && p.kbits != nullptr) {  // k0 is a multiple of 8, so both bits sit in one 32-bit word)
-                    const int k = p.k_begin + t * k2::kKT + 2 * static_cast<int>(lane_id());
-                    const uint32_t* wrow = reinterpret_cast<const uint32_t*>(p.kbits + (size_t)L * (p.I_pad / 64 + 1));
-                    two = wrow[k >> 5] >> (k & 31);
-                }
-                ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it / k2::kStages) & 1) ^ 1, abort));
-                if (!ok) break;
-                if (kEx && p.kbits != nullptr) {  // M of the stage: lane writes keys 2 lane, 2 lane + 1
-                    const uint32_t ln = lane_id();
-                    uint8_t* mt = sm + k2::kStage + st * k2::kStageBytes + k2::kSM + (ln >> 2) * 128 + (ln & 3) * 32;
-                    *reinterpret_cast<uint16_t*>(mt) = (two & 1u) ? uint16_t(0) : uint16_t(0xF753u);   // f16 -30000
-                    *reinterpret_cast<uint16_t*>(mt + 16) = (two & 2u) ? uint16_t(0) : uint16_t(0xF753u);
-                    fence_proxy_async_smem();
+                    uint32_t two = 0;                 // key-valid bits of keys k0 + 2 lane, + 1 (read before the wait;
+                    if (kEx && p.kbits != nullptr) {  // k0 is a multiple of 8, so both bits sit in one 32-bit word)
+                        const int k = p.k_begin + t * k2::kKT + 2 * static_cast<int>(lane_id());
+                        const uint32_t* wrow =
+                            reinterpret_cast<const uint32_t*>(p.kbits + (size_t)L * (p.I_pad / 64 + 1));
+                        two = wrow[k >> 5] >> (k & 31);
+                    }
+                    ok = __all_sync(0xffffffffu, mbar_wait(kv_empty + st, ((it / k2::kStages) & 1) ^ 1, abort));
+                    if (!ok) break;
+                    if (kEx && p.kbits != nullptr) {  // M of the stage: lane writes keys 2 lane, 2 lane + 1
+                        const uint32_t ln = lane_id();
+                        uint8_t* mt =
+                            sm + k2::kStage + st * k2::kStageBytes + k2::kSM + (ln >> 2) * 128 + (ln & 3) * 32;
+                        *reinterpret_cast<uint16_t*>(mt) = (two & 1u) ? uint16_t(0) : uint16_t(0xF753u);   // f16 -30000
+                        *reinterpret_cast<uint16_t*>(mt + 16) = (two & 2u) ? uint16_t(0) : uint16_t(0xF753u);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && item == 0;
+                    if (leader && !skip) {
+                        const int k0 = p.k_begin + t * k2::kKT;
+                        uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
+                        mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
+                        tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
+                        tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
+                    }
+                    if (skip) skipped = it;
+                    it_issued = it + 1;
                     __syncwarp();
                 }
-                const bool skip = p.inject == TRI_ATTN_FAULT_SKIP_STAGE && it == 1 && item == 0;
-                if (leader && !skip) {
-                    const int k0 = p.k_begin + t * k2::kKT;
-                    uint8_t* sb = sm + k2::kStage + st * k2::kStageBytes;
-                    mbar_arrive_expect_tx(kv_full + st, k2::kStageTx);
-                    tma_load_2d(sb + k2::kSK, &mapK, kv_full + st, 0, lh * p.I_pad + k0);
-                    tma_load_2d(sb + k2::kSV, &mapVt, kv_full + st, k0, lh * HD);
-                }
-                if (skip) skipped = it;
-                it_issued = it + 1;
-                __syncwarp();
             }
-          }
         }
         if (fused_out) {
             // the block must not end with the W_o^T copy still writing its shared
@@ -1220,7 +1223,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     tmem_ld32(tS, va);
                     tmem_ld32(tS + 32, vb);
                     tmem_ld_wait();
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         s[i] = __uint_as_float(va[i]);
                         s[32 + i] = __uint_as_float(vb[i]);
@@ -1229,7 +1232,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 const int k0 = p.k_begin + t * k2::kKT;
                 if (k0 + k2::kKT > p.k_end) {                // ragged last tile of the key range
                     const int nvalid = p.k_end - k0;
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < k2::kKT; ++k)
                         if (k >= nvalid) s[k] = -INFINITY;
                 }
@@ -1245,18 +1248,18 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 uint32_t pk[32];
                 if (fast) {
                     const float negm = -m;
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
                 }
                 // tile max: eight independent 3-input max chains
                 float mx[8];
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 8; ++c) mx[c] = max3(s[c], s[8 + c], s[16 + c]);
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[24 + c], s[32 + c]);
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 8; ++c) mx[c] = max3(mx[c], s[40 + c], s[48 + c]);
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], s[56 + c]);
                 const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
                 const bool need = mt > m + 8.f;              // rescale only when the max grew by > 2^8
@@ -1282,7 +1285,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         tmem_ld_wait();
                         const float mn = need ? mt : m;
                         const float alpha = ex2(m - mn);
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
                         lv = __float_as_uint(__uint_as_float(lv) * alpha);
                         tmem_st32(tO, ov);
@@ -1290,7 +1293,7 @@ sm103_attention(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         m = mn;
                     }
                     const float negm = -m;
-    #pragma unroll
+#pragma unroll
                     for (int k = 0; k < k2::kKT; k += 2) pk[k >> 1] = exp2_pair_f16x2(s[k], s[k + 1], negm);
                 } else if (!pv2_done && !mbar_wait(o_ready + g * 2 + b, ((it - 2) >> 1) & 1, abort)) {
                     ok = false;
