@@ -8,16 +8,20 @@
 // from the pair representation).  The operation is stated in tri_attn.h.
 //
 // Kernels per forward:
-//   sm103_msa_prep   folds LayerNorm_m's gamma into W_q | W_k | W_v | W_g (the
-//                    projection GEMM then runs on the raw MSA rows:
-//                    LN(m) W = rstd * (m (gamma.W) - mu * colsum) + beta W),
-//                    the gamma_z-folded pair-bias weights, and W_o^T in f16.
-//   sm103_msa_bias   the pair bias of the 8 heads from Z (LayerNorm_z and 8 dot
-//                    products of length 128 per pair, from a shared-memory copy
-//                    of 64 pairs), log2(e) scaled, f16; padded keys get -30000
-//                    (finite, as on the triangle path: 2^-30000 is 0 in fp32).
-//   sm103_msa_ln_stats  LayerNorm_m mean and 1/std of every (row, residue) slot
-//                    (four threads per slot), and its row of the LayerNorm K-step.
+//   sm103_msa_front  three independent steps in one launch, block ranges side by
+//                    side:
+//                    - weight preparation: folds LayerNorm_m's gamma into W_q |
+//                      W_k | W_v | W_g (the projection GEMM then runs on the raw
+//                      MSA rows: LN(m) W = rstd * (m (gamma.W) - mu * colsum) +
+//                      beta W), and W_o^T in f16;
+//                    - LayerNorm_m mean and 1/std of every (row, residue) slot
+//                      (four threads per slot), and its row of the LayerNorm
+//                      K-step;
+//                    - the pair bias of the 8 heads from Z (LayerNorm_z and 8 dot
+//                      products of length 128 per pair, from a shared-memory copy
+//                      of 64 pairs, with the gamma_z-folded weights formed in the
+//                      block), log2(e) scaled, f16; padded keys get -30000
+//                      (finite, as on the triangle path: 2^-30000 is 0 in fp32).
 //   sm103_msa_gemm<0>  persistent tcgen05 GEMM, one 256-column group (q, k, v
 //                    or gate) per CTA with its 128 KB of weights resident in
 //                    shared memory, 128 MSA slots per tile, K = 256 in 16 MMAs of
@@ -90,20 +94,19 @@ struct MsaPrepArgs {
     const __nv_bfloat16 *w_q, *w_k, *w_v, *w_g, *w_b, *w_o;
     __nv_bfloat16* wprep;   // [1024][256]: row n = (gamma_m . W)[:, n] (q columns x log2(e)/sqrt(d)), K-major
     float* cst;             // [2][1024]: colsum of each column, then its offset
-    float* wb;              // [128][8] gamma_z . W_b, then bcs[8] (column sums), bbw[8] (beta_z W_b)
     __half* wo_t;           // [256][256]: row n = W_o[:, n]
     float* bo;              // [256]
 };
 
-// Blocks 0..31: 32 projection columns each; 32..39: 32 rows of W_o^T each; 40: the
-// pair-bias weights.  The 32-column slab of W (all 256 input channels) is staged
-// in shared memory with coalesced reads; each warp then writes 4 whole K-major
-// rows (512 bytes, one 16-byte group of 8 channels per lane).
+// Prep blocks 0..31: 32 projection columns each; 32..39: 32 rows of W_o^T each.
+// The 32-column slab of W (all 256 input channels) is staged in shared memory
+// with coalesced reads; each warp then writes 4 whole K-major rows (512 bytes,
+// one 16-byte group of 8 channels per lane).
 constexpr int kPrepCols = 32;
+constexpr int kPrepBlocks = NPROJ / kPrepCols + CM / kPrepCols;
 
-__global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
-    __shared__ float tile[CM][kPrepCols + 1];
-    const int blk = blockIdx.x, c = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ void msa_prep_block(const MsaPrepArgs& a, int blk, float (*tile)[kPrepCols + 1]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (blk < NPROJ / kPrepCols) {
         const int n0 = blk * kPrepCols, grp = n0 / CH, col0 = n0 % CH;   // q | k | v | g
         const __nv_bfloat16* W = grp == 0 ? a.w_q : grp == 1 ? a.w_k : grp == 2 ? a.w_v : a.w_g;
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
                 a.cst[NPROJ + n] = bw + (grp == 3 ? a.b_g[col0 + j] : 0.f);
             }
         }
-    } else if (blk < NPROJ / kPrepCols + CM / kPrepCols) {
+    } else {
         const int row0 = (blk - NPROJ / kPrepCols) * kPrepCols;   // output channels of W_o
         for (int cc = warp; cc < CH; cc += 8) tile[cc][lane] = __bfloat162float(a.w_o[(size_t)cc * CM + row0 + lane]);
         __syncthreads();
@@ -145,29 +148,6 @@ __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
             for (int e = 0; e < 8; e += 2) pk[e >> 1] = pack_f16(tile[lane * 8 + e][j], tile[lane * 8 + e + 1][j]);
             reinterpret_cast<uint4*>(a.wo_t + (size_t)row * CH)[lane] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             if (lane == 0) a.bo[row] = a.b_o ? a.b_o[row] : 0.f;
-        }
-    } else {
-        // gamma_z . W_b [128][8], its column sums and beta_z W_b: thread t owns head
-        // t % 8 over channels t / 8 + 32 k, then a reduction over the 32 threads of a head
-        float* bcs = a.wb + CZ * HM;
-        float* bbw = bcs + HM;
-        const int h = c & (HM - 1);
-        float cs = 0.f, b = 0.f;
-        for (int cc = c >> 3; cc < CZ; cc += 32) {
-            const float wv = __bfloat162float(a.w_b[cc * HM + h]);
-            const float g = a.gz[cc] * wv;
-            a.wb[cc * HM + h] = g;
-            cs += g;
-            b = fmaf(a.bz[cc], wv, b);
-        }
-        tile[c >> 3][h] = cs;                      // [32 partials][8 heads], twice
-        tile[32 + (c >> 3)][h] = b;
-        __syncthreads();
-        if (c < 2 * HM) {
-            const int hh = c & (HM - 1), off = c < HM ? 0 : 32;
-            float t = 0.f;
-            for (int k = 0; k < 32; ++k) t += tile[off + k][hh];
-            (c < HM ? bcs : bbw)[hh] = t;
         }
     }
 }
@@ -182,18 +162,29 @@ __global__ void __launch_bounds__(256) sm103_msa_prep(MsaPrepArgs a) {
 // channel) and two of the 8 dot products:
 //   LN(z) . W_b[:, h] = rstd * (z . (gamma W_b)[:, h] - mu * colsum_h) + (beta W_b)_h.
 // The 8 x 64 results are staged again and leave as one 128-byte run per head.
+// Each block first forms gamma_z . W_b, its column sums and beta_z . W_b itself
+// (1024 products; the weight preparation runs in the same launch).
 namespace kb {
 constexpr int kPairs = 64;
 constexpr int kRowBytes = CZ * 2 + 8;        // 264
 }  // namespace kb
 
-__global__ void __launch_bounds__(256) sm103_msa_bias(const __nv_bfloat16* Z, int I, int I_pad, float eps,
-                                                      const float* wb, __half* bias) {
-    __shared__ __align__(16) uint8_t zt[kb::kPairs * kb::kRowBytes];
-    __shared__ __align__(16) float wq[4][CZ][2];           // (gamma_z W_b) by head pair
-    __shared__ __align__(16) __half ob[HM][kb::kPairs];
+struct MsaBiasSmem {
+    __align__(16) uint8_t zt[kb::kPairs * kb::kRowBytes];
+    __align__(16) float wq[4][CZ][2];           // (gamma_z W_b) by head pair
+    __align__(16) __half ob[HM][kb::kPairs];
+    float part[2][32][HM];                      // partial column sums of gamma_z W_b and of beta_z W_b
+    float bsum[2][HM];                          // their totals: bcs (column sums), bbw (beta_z W_b)
+};
+
+__device__ __forceinline__ void msa_bias_block(const __nv_bfloat16* Z, int I, int I_pad, float eps,
+                                               const __nv_bfloat16* w_b, const float* gz, const float* bz,
+                                               __half* bias, int bx, int by, MsaBiasSmem& sb) {
+    auto& zt = sb.zt;
+    auto& wq = sb.wq;
+    auto& ob = sb.ob;
     const int tid = threadIdx.x;
-    const int i = blockIdx.y, j0 = blockIdx.x * kb::kPairs;
+    const int i = by, j0 = bx * kb::kPairs;
     if (i >= I) {                                          // padded query rows: 0
         if (tid < HM * 8) {
             const int h = tid >> 3, c = tid & 7;
@@ -211,10 +202,26 @@ __global__ void __launch_bounds__(256) sm103_msa_bias(const __nv_bfloat16* Z, in
             dst[0] = make_uint2(v.x, v.y);
             dst[1] = make_uint2(v.z, v.w);
         }
-        for (int q = tid; q < CZ * HM; q += 256) {
-            const int c = q / HM, h = q % HM;
-            wq[h >> 1][c][h & 1] = wb[q];
+        // gamma_z . W_b [128][8]: thread t owns head t % 8 over channels t / 8 + 32 k,
+        // with partial column sums (and of beta_z W_b) reduced over the 32 threads of a head
+        const int h = tid & (HM - 1);
+        float cs = 0.f, b = 0.f;
+        for (int cc = tid >> 3; cc < CZ; cc += 32) {
+            const float wv = __bfloat162float(w_b[cc * HM + h]);
+            const float g = gz[cc] * wv;
+            wq[h >> 1][cc][h & 1] = g;
+            cs += g;
+            b = fmaf(bz[cc], wv, b);
         }
+        sb.part[0][tid >> 3][h] = cs;
+        sb.part[1][tid >> 3][h] = b;
+    }
+    __syncthreads();
+    if (tid < 2 * HM) {
+        const int hh = tid & (HM - 1), pl = tid < HM ? 0 : 1;
+        float t = 0.f;
+        for (int k = 0; k < 32; ++k) t += sb.part[pl][k][hh];
+        sb.bsum[pl][hh] = t;
     }
     __syncthreads();
     const int pr = tid & 63, hq = tid >> 6;
@@ -238,8 +245,8 @@ __global__ void __launch_bounds__(256) sm103_msa_bias(const __nv_bfloat16* Z, in
     const float md = sd * (1.f / CZ);
     const float mu = shift + md;
     const float rstd = rsqrtf(fmaxf(sq * (1.f / CZ) - md * md, 0.f) + eps);
-    const float* bcs = wb + CZ * HM;
-    const float* bbw = bcs + HM;
+    const float* bcs = sb.bsum[0];
+    const float* bbw = sb.bsum[1];
     const int h = 2 * hq;
     const bool valid = pr < nj;
     ob[h][pr] = __float2half_rn(valid ? (rstd * (d0 - mu * bcs[h]) + bbw[h]) * kLog2e : kMaskedBias);
@@ -264,9 +271,9 @@ __global__ void __launch_bounds__(256) sm103_msa_bias(const __nv_bfloat16* Z, in
 constexpr int kStatThreads = 256;
 constexpr int kStatSlotsPerBlock = kStatThreads / 4;
 
-__global__ void __launch_bounds__(kStatThreads) sm103_msa_ln_stats(const __nv_bfloat16* M, int S, int I, int I_pad,
-                                                                   float eps, float2* rowstat, uint4* axrow) {
-    const long long slot = (long long)blockIdx.x * kStatSlotsPerBlock + (threadIdx.x >> 2);
+__device__ __forceinline__ void msa_stats_block(const __nv_bfloat16* M, int S, int I, int I_pad, float eps,
+                                                float2* rowstat, uint4* axrow, int blk) {
+    const long long slot = (long long)blk * kStatSlotsPerBlock + (threadIdx.x >> 2);
     const int q = threadIdx.x & 3;
     const long long n_slots = (long long)S * I_pad;
     const bool in = slot < n_slots;
@@ -302,6 +309,43 @@ __global__ void __launch_bounds__(kStatThreads) sm103_msa_ln_stats(const __nv_bf
     // bf16 (hi, lo) pairs, sd = sqrt(var) = 1 / rstd
     const uint32_t m2 = split_bf16(-mu), s2 = split_bf16(live ? sqrtf(var) : 1.f);
     axrow[slot] = make_uint4(m2, m2, s2, s2);
+}
+
+// =====================================================================================
+// The three front steps of an MSA forward in one launch: they are independent of
+// one another (each pair-bias block forms its own gamma_z-folded weights), so the
+// weight preparation, the pair bias over Z and the LayerNorm_m statistics over the
+// MSA rows share the GPU instead of running one after the other.  Blocks
+// [0, kPrepBlocks) prepare weights, then n_stat blocks of statistics (64 slots
+// each), then one pair-bias block per (64 keys, query row).
+// =====================================================================================
+struct MsaFrontArgs {
+    MsaPrepArgs prep;
+    const __nv_bfloat16 *M, *Z;
+    int S, I, I_pad, n_stat, n_bias_x;
+    float eps;
+    float2* rowstat;
+    uint4* axrow;
+    __half* bias;
+};
+union MsaFrontSmem {
+    float prep_tile[CM][kPrepCols + 1];
+    MsaBiasSmem bias;
+};
+static_assert(kStatThreads == 256, "one block size for the fused front steps");
+
+__global__ void __launch_bounds__(256) sm103_msa_front(MsaFrontArgs a) {
+    __shared__ MsaFrontSmem sh;
+    const int blk = blockIdx.x;
+    if (blk < kPrepBlocks) {
+        msa_prep_block(a.prep, blk, sh.prep_tile);
+    } else if (blk < kPrepBlocks + a.n_stat) {
+        msa_stats_block(a.M, a.S, a.I, a.I_pad, a.eps, a.rowstat, a.axrow, blk - kPrepBlocks);
+    } else {
+        const int b = blk - kPrepBlocks - a.n_stat;
+        msa_bias_block(a.Z, a.I, a.I_pad, a.eps, a.prep.w_b, a.prep.gz, a.prep.bz, a.bias, b % a.n_bias_x,
+                       b / a.n_bias_x, sh.bias);
+    }
 }
 
 // =====================================================================================
@@ -671,28 +715,23 @@ cudaError_t sm103_msa_forward(const MsaArgs& a, cudaStream_t s, LaunchTimer* tm)
                    static_cast<const __nv_bfloat16*>(a.w.w_q), static_cast<const __nv_bfloat16*>(a.w.w_k),
                    static_cast<const __nv_bfloat16*>(a.w.w_v), static_cast<const __nv_bfloat16*>(a.w.w_g),
                    static_cast<const __nv_bfloat16*>(a.w.w_b), static_cast<const __nv_bfloat16*>(a.w.w_o),
-                   reinterpret_cast<__nv_bfloat16*>(ws + W.wprep), f32(W.cst), f32(W.wb32), hf(W.wo_t), f32(W.bo)};
-    if (tm) tm->begin("sm103_msa_prep", s);
-    sm103_msa_prep<<<NPROJ / kPrepCols + CM / kPrepCols + 1, 256, 0, s>>>(pa);
-    if (tm) tm->end(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-    // ---- pair bias of the 8 heads
+                   reinterpret_cast<__nv_bfloat16*>(ws + W.wprep), f32(W.cst), hf(W.wo_t), f32(W.bo)};
     {
-        if (tm) tm->begin("sm103_msa_bias", s);
-        sm103_msa_bias<<<dim3(Ip / kb::kPairs, Ip), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.Z), I, Ip, a.eps,
-                                                                f32(W.wb32), hf(W.bias));
-        if (tm) tm->end(s);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-
-    // ---- LayerNorm_m statistics of every slot
-    {
-        const long long blocks = ((long long)S * Ip + kStatSlotsPerBlock - 1) / kStatSlotsPerBlock;
-        if (tm) tm->begin("sm103_msa_ln_stats", s);
-        sm103_msa_ln_stats<<<(unsigned)blocks, kStatThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(a.M), S, I, Ip,
-                                                                       a.eps, reinterpret_cast<float2*>(ws + W.rowstat),
-                                                                       reinterpret_cast<uint4*>(ws + W.axrow));
+        MsaFrontArgs fa{pa,
+                        static_cast<const __nv_bfloat16*>(a.M),
+                        static_cast<const __nv_bfloat16*>(a.Z),
+                        S,
+                        I,
+                        Ip,
+                        (int)(((long long)S * Ip + kStatSlotsPerBlock - 1) / kStatSlotsPerBlock),
+                        Ip / kb::kPairs,
+                        a.eps,
+                        reinterpret_cast<float2*>(ws + W.rowstat),
+                        reinterpret_cast<uint4*>(ws + W.axrow),
+                        hf(W.bias)};
+        const long long blocks = (long long)kPrepBlocks + fa.n_stat + (long long)fa.n_bias_x * Ip;
+        if (tm) tm->begin("sm103_msa_front", s);
+        sm103_msa_front<<<(unsigned)blocks, 256, 0, s>>>(fa);
         if (tm) tm->end(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -147,7 +147,6 @@ constexpr Workspace sm103_msa_layout(int S, int I, int key_chunks) {
     auto take = [&off](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
     w.wprep = take((size_t)1024 * 256 * 2);           // (gamma_m . W)^T for q | k | v | g, bf16
     w.cst = take((size_t)2 * 1024 * 4);               // column sums, then offsets, of the 1024 columns
-    w.wb32 = take((size_t)128 * 8 * 4 + 2 * 8 * 4);   // gamma_z . W_b, its column sums, beta_z W_b
     w.wo_t = take((size_t)256 * 256 * 2);             // W_o^T, f16
     w.bo = take(256 * 4);
     w.kbits = take((size_t)S * (w.I_pad / 64 + 1) * 8);
