@@ -296,7 +296,8 @@ int tri_attn_kernel_times(tri_attn_ctx* ctx, const char** names, float* ms, int 
  * the primary context) looks it up with cudaGetSymbolAddress and caches it
  * under the context's id, so make that first call before any stream capture.
  * Every call shares the one array and leaves its contents behind; the status
- * word inside it is cleared (on the stream) at the start of each call.  Calls
+ * word inside it is cleared (on the stream) at the start of each call, and the
+ * attention kernel's work-item counter before each of its launches.  Calls
  * whose work overlaps on the GPU race on the array: issue them on one stream,
  * or otherwise order them. */
 tri_attn_status tri_attn_forward_static(int node, int I, const void* Z, const uint8_t* token_mask,
@@ -307,8 +308,8 @@ tri_attn_status tri_attn_forward_static(int node, int I, const void* Z, const ui
  * array and clears it.  Returns ETIMEOUT if a device-side bounded wait of that
  * call gave up (its `out` is then incomplete), else ERANGE if an f16
  * intermediate left the f16 range (as for tri_attn_status_sync), ECUDA if the
- * stream or the copy reports an error, else OK.  Call it before the next static call (which clears
- * the word). */
+ * stream or the copy reports an error, else OK.  Call it before the next
+ * static call (which clears the word). */
 tri_attn_status tri_attn_static_status(void* stream);
 
 /* Test hook for the failure path (no GPU fault is involved).
