@@ -153,9 +153,11 @@ constexpr int kStatSlotsPerBlock = kStatThreads / 4;
 __global__ void __launch_bounds__(kStatThreads) sm103_tf32_stats(const float* Z, int node, int I, int I_pad, float eps,
                                                                  const uint8_t* mask, const float* wb, float2* rowstat,
                                                                  uint4* ax0, uint4* ax1, __half* bias) {
-    __shared__ float4 swb[CZ];                    // (gamma W_b)[c][0..3]
+    // (gamma W_b)[c][0..3] at c + c / 8: one 16-byte pad per 8 channels puts the four
+    // channels that the four threads of a slot read at once in different banks
+    __shared__ float4 swb[CZ + CZ / 8];
     __shared__ float sbc[2 * NH];
-    for (int i = threadIdx.x; i < CZ; i += blockDim.x) swb[i] = reinterpret_cast<const float4*>(wb)[i];
+    for (int i = threadIdx.x; i < CZ; i += blockDim.x) swb[i + (i >> 3)] = reinterpret_cast<const float4*>(wb)[i];
     if (threadIdx.x < 2 * NH) sbc[threadIdx.x] = wb[CZ * NH + threadIdx.x];
     __syncthreads();
     const long long slot = (long long)blockIdx.x * kStatSlotsPerBlock + (threadIdx.x >> 2);
@@ -176,7 +178,8 @@ __global__ void __launch_bounds__(kStatThreads) sm103_tf32_stats(const float* Z,
         const float z[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float4 w = swb[4 * (qtr + 4 * i) + e];
+            const int ch = 4 * (qtr + 4 * i) + e;
+            const float4 w = swb[ch + (ch >> 3)];
             const float dz = z[e] - shift;
             sd += dz;
             sq = fmaf(dz, dz, sq);
