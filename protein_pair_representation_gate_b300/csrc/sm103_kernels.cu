@@ -181,7 +181,8 @@ constexpr int kBar = kConst + ((kConstBytes + 127) / 128) * 128;
 // swizzle) per warp of those three warpgroups.
 constexpr int kStg = ((kBar + 256 + 1023) / 1024) * 1024;
 constexpr int kStgWarp = 2048;
-constexpr int kSmem = kStg + 12 * kStgWarp + 1024;   // + alignment slack
+constexpr int kStat = kStg + 12 * kStgWarp;  // (mu, rstd) of the tile's 128 rows, 2 buffers (warpgroup 0 -> 1..3)
+constexpr int kSmem = kStat + 2 * 128 * 8 + 1024;   // + alignment slack
 static_assert(kSmem <= 232448, "dynamic shared memory above the per-block limit");
 }  // namespace k1
 
@@ -204,6 +205,8 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
     uint64_t* acc_empty = bars + 7;   // [2]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10);
     volatile int* abort = reinterpret_cast<volatile int*>(bars + 11);
+    uint64_t* stat_full = bars + 12;  // [2]: warpgroup 0 has written the tile's (mu, rstd)
+    float2* s_stat = reinterpret_cast<float2*>(sm + k1::kStat);   // [2][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < 256 * 4; i += blockDim.x) s_cst[i] = p.cst[i];
@@ -219,6 +222,7 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
             mbar_init(z_empty + s, 1 + 16);       // MMA commit + 16 epilogue warps
             mbar_init(acc_full + s, 1);
             mbar_init(acc_empty + s, 8);          // the two warpgroups reading this half
+            mbar_init(stat_full + s, 4);          // the four warps of warpgroup 0
         }
         *abort = 0;
         fence_mbar_init();
@@ -306,36 +310,69 @@ sm103_ln_proj(const __grid_constant__ CUtensorMap mapZs, const __grid_constant__
                 set_abort(abort, p.status, kStatusTimeoutEpilogue);
                 break;
             }
-            // LayerNorm statistics of the raw pair vector in one pass over its SMEM row,
-            // shifted by its first channel (exact algebra; avoids cancellation when
-            // the mean is large against the spread), and z . (gamma W_b)[:, wg] for
-            // this warpgroup's head in the same pass.
+            // Warpgroup 0 forms the LayerNorm statistics of the raw pair vector in one
+            // pass over its SMEM row, shifted by its first channel (exact algebra; avoids
+            // cancellation when the mean is large against the spread), and hands them to
+            // the other three through shared memory; every warpgroup forms
+            // z . (gamma W_b)[:, wg] for its head in its own pass.  The other warpgroups
+            // release the Z stage only after reading the statistics, so the buffer of
+            // tile j is rewritten (at tile j + 2, after that stage's release) only once
+            // all have read it.
             const uint8_t* zb = sm + k1::kZ + s * 32768 + r * 128;
-            const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(zb + ((0 ^ (r & 7)) << 4)));
-            float sd = 0.f, sq = 0.f, bh = 0.f;
+            float mu, rstd, bh = 0.f;
+            if (wg == 0) {
+                const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(zb + ((0 ^ (r & 7)) << 4)));
+                float sd = 0.f, sq = 0.f;
 #pragma unroll 2
-            for (int cc = 0; cc < 16; ++cc) {
-                const int b = cc >> 3, c = cc & 7;
-                const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
-                const float4 wa = *reinterpret_cast<const float4*>(wbt + cc * 8);
-                const float4 wb = *reinterpret_cast<const float4*>(wbt + cc * 8 + 4);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                for (int cc = 0; cc < 16; ++cc) {
+                    const int b = cc >> 3, c = cc & 7;
+                    const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
+                    const float4 wa = *reinterpret_cast<const float4*>(wbt + cc * 8);
+                    const float4 wb = *reinterpret_cast<const float4*>(wbt + cc * 8 + 4);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    const float z0 = bf16lo(w4[q2]), z1 = bf16hi(w4[q2]);
-                    const float d0 = z0 - shift, d1 = z1 - shift;
-                    sd += d0 + d1;
-                    sq = fmaf(d0, d0, fmaf(d1, d1, sq));
-                    bh = fmaf(z0, wv[2 * q2], fmaf(z1, wv[2 * q2 + 1], bh));
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const float z0 = bf16lo(w4[q2]), z1 = bf16hi(w4[q2]);
+                        const float d0 = z0 - shift, d1 = z1 - shift;
+                        sd += d0 + d1;
+                        sq = fmaf(d0, d0, fmaf(d1, d1, sq));
+                        bh = fmaf(z0, wv[2 * q2], fmaf(z1, wv[2 * q2 + 1], bh));
+                    }
                 }
+                const float md = sd * (1.f / CZ);
+                mu = shift + md;
+                const float var = fmaxf(sq * (1.f / CZ) - md * md, 0.f);
+                rstd = rsqrtf(var + p.eps);
+                s_stat[s * 128 + r] = make_float2(mu, rstd);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(stat_full + s);
+                    mbar_arrive(z_empty + s);
+                }
+            } else {
+#pragma unroll 2
+                for (int cc = 0; cc < 16; ++cc) {
+                    const int b = cc >> 3, c = cc & 7;
+                    const uint4 v = *reinterpret_cast<const uint4*>(zb + b * 16384 + ((c ^ (r & 7)) << 4));
+                    const float4 wa = *reinterpret_cast<const float4*>(wbt + cc * 8);
+                    const float4 wb = *reinterpret_cast<const float4*>(wbt + cc * 8 + 4);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2)
+                        bh = fmaf(bf16lo(w4[q2]), wv[2 * q2], fmaf(bf16hi(w4[q2]), wv[2 * q2 + 1], bh));
+                }
+                if (!mbar_wait(stat_full + s, (j >> 1) & 1, abort)) {
+                    set_abort(abort, p.status, kStatusTimeoutEpilogue);
+                    break;
+                }
+                const float2 st = s_stat[s * 128 + r];
+                mu = st.x;
+                rstd = st.y;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(z_empty + s);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(z_empty + s);
-            const float md = sd * (1.f / CZ);
-            const float mu = shift + md;
-            const float var = fmaxf(sq * (1.f / CZ) - md * md, 0.f);
-            const float rstd = rsqrtf(var + p.eps);
             {
                 // pair bias of head wg: rstd * (z . gW_b[:, h] - mu * colsum) + beta W_b, in log2 units
                 const bool valid = x < p.I && (p.mask == nullptr || p.mask[x] != 0);
